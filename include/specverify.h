@@ -1,0 +1,189 @@
+/*
+ * specverify: target-side verification step of speculative decoding on one
+ * GB300 (sm_103a).  C ABI of libspecverify.so.
+ *
+ * The operation (every entry point computes some part of it):
+ *   Given target logits z for B requests x (K+1) positions over a vocabulary
+ *   of V tokens, draft probabilities q for the K drafted positions, the
+ *   drafted ids x_0..x_{K-1} and uniforms u_0..u_K of each request:
+ *     p_j = softmax(z_j / T)                       ("Speculative Decoding"
+ *           glossary, "Mathematical Guarantee"; T = 0 selects greedy)
+ *     accept x_j iff u_j <= min(1, p_j(x_j) / q_j(x_j)), evaluated as
+ *           u_j * q_j(x_j) <= p_j(x_j)              ("Speculative Decoding in
+ *           Large Language Models", section 2, "Modified Rejection Sampling")
+ *     k* = the first rejected position, or K        ("Co-Designing AI Models
+ *           Using Speculative Decoding", "What is speculative decoding?")
+ *     emit x_0..x_{k*-1}, then one token drawn with the final uniform u_K from
+ *           max(0, p_k* - q_k*) / sum max(0, p_k* - q_k*) when k* < K
+ *           (section 2, residual p'(x)), or from p_K when every draft was
+ *           accepted (the target always produces one more token, so the
+ *           accepted length AL = k* + 1 lies in [1, 1 + K]).
+ *   Greedy mode accepts while x_j == argmax_v z_j(v) (lowest index on ties)
+ *   and emits argmax z_k* at the stop; its output equals plain argmax
+ *   decoding ("Co-Designing...", "What is speculative decoding?").
+ *   The draw from a distribution r is an inverse CDF in ascending token
+ *   index: the smallest v with sum_{w<=v} r(w) > u_K * sum_w r(w); if rounding
+ *   leaves none, the largest v with r(v) > 0.  If the residual is empty after
+ *   a rejection (only possible through rounding) the draw uses p_k* instead
+ *   and the device status word records it (SV_FLAG_ZERO_RESIDUAL).
+ *
+ * Conventions shared by every entry point:
+ *   - Every data pointer is caller-owned DEVICE memory, row-major, densely
+ *     packed.  The library never allocates device or host memory on these
+ *     paths and keeps no per-call state outside the caller's workspace.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are stream-ordered and asynchronous; nothing
+ *     synchronises the host except spec_verify_last_device_status().
+ *   - Argument errors are detected on the host before any launch and return
+ *     SV_ERR_INVALID (bad sizes, null pointers, T <= 0 in sampling mode,
+ *     K > SV_MAX_K) or SV_ERR_WORKSPACE; nothing is launched then.
+ *   - Input errors only the device can see (a drafted id outside [0, V),
+ *     malformed CSR offsets) set bits of a status word kept in the workspace;
+ *     the affected request gets AL = 0 and all its output slots -1, the others
+ *     are unaffected.  spec_verify_last_device_status() reads and clears it.
+ *     No kernel traps.
+ *   - Layout of a request b with K_b drafts and first logits row r_b:
+ *       logits rows r_b .. r_b + K_b            (position j = row r_b + j)
+ *       q rows / draft ids  r_b - b .. r_b - b + K_b - 1
+ *       uniforms, out_tokens  r_b .. r_b + K_b  (u_j, j < K_b accept draws;
+ *                                                u_{K_b} the final draw)
+ *     Fixed-K calls use r_b = b (K+1).  Output slots past AL hold -1.
+ *   - A workspace may not be shared by calls that overlap on the device.
+ *     It needs no initialisation: every call leaves it reusable, even one
+ *     that reported a device input error.
+ *   - `diag` (may be NULL) receives per-token diagnostics in fp32:
+ *       diag[i], i < Nq = rows - B : p_j(x_j) of draft slot i
+ *       diag[Nq + 2b]              : mass R of the distribution the final
+ *                                    token of request b was drawn from
+ *       diag[Nq + 2b + 1]          : r(v*) / R, the probability of the token
+ *                                    that was drawn
+ *     In greedy mode diag is ignored.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sv_status {
+    SV_OK = 0,
+    SV_ERR_INVALID = 1,      /* bad argument, found on the host; nothing launched */
+    SV_ERR_CUDA = 2,         /* a CUDA runtime call or launch failed */
+    SV_ERR_DEVICE_INPUT = 3, /* device-detected input error (status word) */
+    SV_ERR_TIMEOUT = 4,      /* a bounded device-side wait gave up */
+    SV_ERR_WORKSPACE = 5     /* workspace too small or not 256-byte aligned */
+} sv_status;
+
+typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+/* Bits of the device status word. */
+#define SV_FLAG_BAD_TOKEN 0x1u      /* a drafted id outside [0, V) */
+#define SV_FLAG_BAD_OFFSETS 0x2u    /* CSR offsets not increasing, or K_b > SV_MAX_K */
+#define SV_FLAG_ZERO_RESIDUAL 0x4u  /* informational: a draw fell back to p */
+#define SV_FLAG_TIMEOUT 0x8u        /* a bounded wait expired */
+
+/* Largest number of drafted tokens per request. */
+#define SV_MAX_K 255
+
+/*
+ * Bytes of workspace a call over B requests, `rows` logits rows in total
+ * (B (K+1) for fixed K) and vocabulary V needs.  Pure host function.
+ */
+size_t spec_verify_workspace_size(int B, int rows, int V);
+
+/*
+ * Greedy verification ("Co-Designing...", "What is speculative decoding?").
+ *   logits     (B (K+1)) x V, dtype dt
+ *   draft      B K int32 ids
+ *   out_tokens B (K+1) int32;  accept_len  B int32 (AL per request)
+ *   ws         spec_verify_workspace_size(B, B (K+1), V) bytes, 256-aligned
+ * Bit-exact: argmax is taken on the logits as stored, ties to the lowest id.
+ */
+sv_status spec_verify_greedy(const void *logits, sv_dtype dt, int B, int K, int V,
+                             const int32_t *draft, int32_t *out_tokens, int32_t *accept_len,
+                             void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Sampling verification ("Speculative Decoding in Large Language Models",
+ * section 2 "Modified Rejection Sampling"; the glossary's "Mathematical
+ * Guarantee"; page-4 equations for alpha and P').
+ *   logits      (B (K+1)) x V, dtype dt;   q  (B K) x V fp32 (already tempered)
+ *   temperature T > 0;  draft B K int32;  uniforms B (K+1) fp32 in (0, 1)
+ *   out_tokens  B (K+1) int32;  accept_len B int32;  diag see above
+ */
+sv_status spec_verify_sample(const void *logits, sv_dtype dt, const float *q, int B, int K,
+                             int V, float temperature, const int32_t *draft,
+                             const float *uniforms, int32_t *out_tokens, int32_t *accept_len,
+                             float *diag, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Per-request draft lengths K_b ("Hardware Aware Dynamic Speculative
+ * Decoding": K chosen per batch at run time), given as CSR row offsets.
+ *   row_offsets B+1 int32 on the device: row_offsets[0] = 0,
+ *               row_offsets[b+1] - row_offsets[b] = K_b + 1 in [1, SV_MAX_K+1]
+ *   rows        row_offsets[B] (the caller's host-side copy of it; the device
+ *               checks that they agree)
+ *   logits rows x V;  q (rows - B) x V fp32;  draft rows - B;  uniforms rows;
+ *   out_tokens rows;  accept_len B.   temperature 0 = greedy (q, uniforms,
+ *   diag then unused), else sampling.
+ */
+sv_status spec_verify_ragged(const void *logits, sv_dtype dt, const float *q,
+                             const int32_t *row_offsets, int B, int rows, int V,
+                             float temperature, const int32_t *draft, const float *uniforms,
+                             int32_t *out_tokens, int32_t *accept_len, float *diag, void *ws,
+                             size_t ws_bytes, void *stream);
+
+/*
+ * Bytes of workspace spec_lmhead_verify needs for M = B (K+1) rows, hidden
+ * size d and vocabulary V (it includes an fp32 M x V spill of the tile
+ * logits that only the selected rows are read back from).
+ */
+size_t spec_lmhead_workspace_size(int B, int K, int d, int V);
+
+/*
+ * Fused LM-head front end + verification.  The target logits are the
+ * product z = hidden . W_vocab (bf16 operands, fp32 accumulation on the
+ * tensor cores) and feed the verifier tile by tile; this is the GEMM whose M
+ * grows from B to B (1 + D) under speculation ("Co-Designing...", Guideline 1).
+ *   hidden     M x d bf16, M = B (K+1) <= 128, d a multiple of 64
+ *   w_vocab_t  V x d bf16: W_vocab stored transposed (row v = the d weights
+ *              of token v, the layout of a Linear layer's weight); V % 16 == 0
+ *   q, draft, uniforms, out_tokens, accept_len, diag as in spec_verify_sample
+ *   temperature 0 = greedy, else sampling
+ */
+sv_status spec_lmhead_verify(const void *hidden, const void *w_vocab_t, int d, const float *q,
+                             int B, int K, int V, float temperature, const int32_t *draft,
+                             const float *uniforms, int32_t *out_tokens, int32_t *accept_len,
+                             float *diag, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Synchronises `stream`, returns the device status word of workspace `ws`
+ * in *flags (SV_FLAG_* bits, may be NULL) and clears it.  Returns
+ * SV_ERR_DEVICE_INPUT if an input-error bit was set, SV_ERR_TIMEOUT if the
+ * timeout bit was set, SV_ERR_CUDA on a CUDA error, else SV_OK.
+ */
+sv_status spec_verify_last_device_status(void *ws, void *stream, uint32_t *flags);
+
+/* Human-readable name of a status code (static storage). */
+const char *spec_status_string(sv_status s);
+
+/*
+ * Profiling hook: when `begin` and `end` are non-NULL cudaEvent_t handles,
+ * every later call records `begin` just before its dominant kernel (the
+ * logits-streaming pass, or the LM-head GEMM) and `end` just after it, on the
+ * call's stream.  Pass NULL, NULL to stop.  Process-wide; not thread-safe.
+ */
+sv_status spec_profile_set_events(void *begin, void *end);
+
+/* Number of kernels the last call on this thread launched (for accounting). */
+int spec_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -1,0 +1,203 @@
+"""Thin Python binding of libspecverify.so (ctypes).
+
+Argument marshalling only: every function passes device pointers, sizes and
+the current CUDA stream straight to the C entry point of the same name in
+``include/specverify.h``.  No step of the verification runs here, and there is
+no CPU fallback: if the library is missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+SV_OK, SV_ERR_INVALID, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, SV_ERR_TIMEOUT, SV_ERR_WORKSPACE = range(6)
+SV_F32, SV_BF16 = 0, 1
+SV_FLAG_BAD_TOKEN, SV_FLAG_BAD_OFFSETS, SV_FLAG_ZERO_RESIDUAL, SV_FLAG_TIMEOUT = 1, 2, 4, 8
+SV_MAX_K = 255
+
+EXPORTS = (
+    "spec_verify_workspace_size", "spec_verify_greedy", "spec_verify_sample", "spec_verify_ragged",
+    "spec_lmhead_workspace_size", "spec_lmhead_verify", "spec_verify_last_device_status",
+    "spec_status_string", "spec_profile_set_events", "spec_last_launch_count",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load the built library (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        sig = {
+            "spec_verify_workspace_size": (Z, [I, I, I]),
+            "spec_verify_greedy": (I, [P, I, I, I, I, P, P, P, P, Z, P]),
+            "spec_verify_sample": (I, [P, I, P, I, I, I, F, P, P, P, P, P, P, Z, P]),
+            "spec_verify_ragged": (I, [P, I, P, P, I, I, I, F, P, P, P, P, P, P, Z, P]),
+            "spec_lmhead_workspace_size": (Z, [I, I, I, I]),
+            "spec_lmhead_verify": (I, [P, P, I, P, I, I, I, F, P, P, P, P, P, P, Z, P]),
+            "spec_verify_last_device_status": (I, [P, P, P]),
+            "spec_status_string": (ctypes.c_char_p, [I]),
+            "spec_profile_set_events": (I, [P, P]),
+            "spec_last_launch_count": (I, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().spec_status_string(int(status)).decode()
+    except Exception:  # library not loadable: plain number
+        return f"status {status}"
+
+
+# --------------------------------------------------------------------------
+# marshalling helpers
+# --------------------------------------------------------------------------
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to libspecverify must live on the GPU")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libspecverify must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, dtype, numel=None, name="tensor"):
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name}: expected {numel} elements, got {t.numel()}")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.float32:
+        return SV_F32
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    raise TypeError(f"logits must be fp32 or bf16, got {t.dtype}")
+
+
+def _raise(status, where):
+    if status != SV_OK:
+        raise SpecVerifyError(status, where)
+
+
+# --------------------------------------------------------------------------
+# the C entry points, same names
+# --------------------------------------------------------------------------
+def spec_verify_workspace_size(B: int, rows: int, V: int) -> int:
+    return int(load().spec_verify_workspace_size(B, rows, V))
+
+
+def spec_lmhead_workspace_size(B: int, K: int, d: int, V: int) -> int:
+    return int(load().spec_lmhead_workspace_size(B, K, d, V))
+
+
+def spec_verify_greedy(logits, draft, B, K, V, out_tokens, accept_len, ws, stream=None):
+    _check(draft, torch.int32, B * K, "draft")
+    _check(out_tokens, torch.int32, B * (K + 1), "out_tokens")
+    _check(accept_len, torch.int32, B, "accept_len")
+    st = load().spec_verify_greedy(_ptr(logits), _dtype_code(logits), B, K, V, _ptr(draft),
+                                   _ptr(out_tokens), _ptr(accept_len), _ptr(ws), ws.numel(),
+                                   _stream(stream))
+    _raise(st, "spec_verify_greedy")
+
+
+def spec_verify_sample(logits, q, B, K, V, temperature, draft, uniforms, out_tokens, accept_len,
+                       ws, diag=None, stream=None):
+    _check(q, torch.float32, B * K * V, "q")
+    _check(draft, torch.int32, B * K, "draft")
+    _check(uniforms, torch.float32, B * (K + 1), "uniforms")
+    _check(out_tokens, torch.int32, B * (K + 1), "out_tokens")
+    _check(accept_len, torch.int32, B, "accept_len")
+    st = load().spec_verify_sample(_ptr(logits), _dtype_code(logits), _ptr(q), B, K, V,
+                                   float(temperature), _ptr(draft), _ptr(uniforms),
+                                   _ptr(out_tokens), _ptr(accept_len), _ptr(diag), _ptr(ws),
+                                   ws.numel(), _stream(stream))
+    _raise(st, "spec_verify_sample")
+
+
+def spec_verify_ragged(logits, q, row_offsets, B, rows, V, temperature, draft, uniforms,
+                       out_tokens, accept_len, ws, diag=None, stream=None):
+    _check(row_offsets, torch.int32, B + 1, "row_offsets")
+    _check(out_tokens, torch.int32, rows, "out_tokens")
+    _check(accept_len, torch.int32, B, "accept_len")
+    st = load().spec_verify_ragged(_ptr(logits), _dtype_code(logits), _ptr(q), _ptr(row_offsets),
+                                   B, rows, V, float(temperature), _ptr(draft), _ptr(uniforms),
+                                   _ptr(out_tokens), _ptr(accept_len), _ptr(diag), _ptr(ws),
+                                   ws.numel(), _stream(stream))
+    _raise(st, "spec_verify_ragged")
+
+
+def spec_lmhead_verify(hidden, w_vocab_t, d, q, B, K, V, temperature, draft, uniforms,
+                       out_tokens, accept_len, ws, diag=None, stream=None):
+    _check(hidden, torch.bfloat16, B * (K + 1) * d, "hidden")
+    _check(w_vocab_t, torch.bfloat16, V * d, "w_vocab_t")
+    _check(out_tokens, torch.int32, B * (K + 1), "out_tokens")
+    _check(accept_len, torch.int32, B, "accept_len")
+    st = load().spec_lmhead_verify(_ptr(hidden), _ptr(w_vocab_t), d, _ptr(q), B, K, V,
+                                   float(temperature), _ptr(draft), _ptr(uniforms),
+                                   _ptr(out_tokens), _ptr(accept_len), _ptr(diag), _ptr(ws),
+                                   ws.numel(), _stream(stream))
+    _raise(st, "spec_lmhead_verify")
+
+
+def spec_verify_last_device_status(ws, stream=None):
+    """Returns (status, flags); synchronises the stream and clears the word."""
+    flags = ctypes.c_uint32(0)
+    st = load().spec_verify_last_device_status(_ptr(ws), _stream(stream), ctypes.byref(flags))
+    return int(st), int(flags.value)
+
+
+def spec_profile_set_events(begin=None, end=None):
+    b = ctypes.c_void_p(begin.cuda_event) if begin is not None else None
+    e = ctypes.c_void_p(end.cuda_event) if end is not None else None
+    _raise(load().spec_profile_set_events(b, e), "spec_profile_set_events")
+
+
+def spec_last_launch_count() -> int:
+    return int(load().spec_last_launch_count())
+
+
+def workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A 256-byte aligned device buffer of nbytes (uint8) from torch's allocator."""
+    t = torch.zeros(nbytes + 256, dtype=torch.uint8, device=device or "cuda")
+    off = (-t.data_ptr()) % 256
+    return t[off:off + nbytes]

@@ -1,0 +1,12 @@
+// Host-side helpers shared by the translation units of libspecverify.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sv {
+uint32_t next_epoch();             // unique tag of one call (tickets compare it)
+void prof_begin(cudaStream_t s);   // profiling hook around the dominant kernel
+void prof_end(cudaStream_t s);
+void set_launches(int n);          // kernels launched by the last call (this thread)
+}  // namespace sv

@@ -1,0 +1,106 @@
+"""Host-side checks of the C ABI (no GPU): the library builds for sm_103a,
+loads, exports every entry point the header declares, and rejects bad
+arguments before any launch."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decoding_verification_11_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def test_header_and_binding_agree():
+    assert sorted(binding.EXPORTS) == _declared()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.spec_status_string(code)
+    assert lib.spec_status_string(99) == b"unknown status"
+
+
+def test_workspace_size_grows_with_problem(lib):
+    small = lib.spec_verify_workspace_size(64, 320, 128256)
+    big = lib.spec_verify_workspace_size(256, 1280, 151936)
+    assert small % 256 == 0 and big > small
+    # partials: one (M, s) pair per 8192-token chunk of every row
+    assert small >= 320 * 16 * 8
+
+
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails on the host
+ALIGNED_WS = ctypes.c_void_p(0x10000)
+
+
+def test_argument_errors_return_before_launch(lib):
+    I = binding
+    ws_bytes = 1 << 20
+    # K out of range
+    assert lib.spec_verify_greedy(FAKE, 0, 4, -1, 100, FAKE, FAKE, FAKE, ALIGNED_WS, ws_bytes, None) == I.SV_ERR_INVALID
+    assert lib.spec_verify_greedy(FAKE, 0, 4, 256, 100, FAKE, FAKE, FAKE, ALIGNED_WS, ws_bytes, None) == I.SV_ERR_INVALID
+    # bad dtype, bad V, null logits
+    assert lib.spec_verify_greedy(FAKE, 7, 4, 2, 100, FAKE, FAKE, FAKE, ALIGNED_WS, ws_bytes, None) == I.SV_ERR_INVALID
+    assert lib.spec_verify_greedy(FAKE, 0, 4, 2, 0, FAKE, FAKE, FAKE, ALIGNED_WS, ws_bytes, None) == I.SV_ERR_INVALID
+    assert lib.spec_verify_greedy(None, 0, 4, 2, 100, FAKE, FAKE, FAKE, ALIGNED_WS, ws_bytes, None) == I.SV_ERR_INVALID
+    # sampling needs T > 0 and finite, uniforms and q
+    for T in (0.0, -1.0, float("inf"), float("nan")):
+        assert lib.spec_verify_sample(FAKE, 0, FAKE, 4, 2, 100, T, FAKE, FAKE, FAKE, FAKE, None,
+                                      ALIGNED_WS, ws_bytes, None) == I.SV_ERR_INVALID
+    assert lib.spec_verify_sample(FAKE, 0, None, 4, 2, 100, 1.0, FAKE, FAKE, FAKE, FAKE, None,
+                                  ALIGNED_WS, ws_bytes, None) == I.SV_ERR_INVALID
+    assert lib.spec_verify_sample(FAKE, 0, FAKE, 4, 2, 100, 1.0, FAKE, None, FAKE, FAKE, None,
+                                  ALIGNED_WS, ws_bytes, None) == I.SV_ERR_INVALID
+    # ragged: null offsets, negative temperature
+    assert lib.spec_verify_ragged(FAKE, 0, FAKE, None, 4, 10, 100, 1.0, FAKE, FAKE, FAKE, FAKE, None,
+                                  ALIGNED_WS, ws_bytes, None) == I.SV_ERR_INVALID
+    assert lib.spec_verify_ragged(FAKE, 0, FAKE, FAKE, 4, 10, 100, -0.5, FAKE, FAKE, FAKE, FAKE, None,
+                                  ALIGNED_WS, ws_bytes, None) == I.SV_ERR_INVALID
+    # rows fewer than requests
+    assert lib.spec_verify_ragged(FAKE, 0, FAKE, FAKE, 4, 3, 100, 1.0, FAKE, FAKE, FAKE, FAKE, None,
+                                  ALIGNED_WS, ws_bytes, None) == I.SV_ERR_INVALID
+
+
+def test_workspace_errors(lib):
+    I = binding
+    need = lib.spec_verify_workspace_size(4, 12, 100)
+    assert lib.spec_verify_greedy(FAKE, 0, 4, 2, 100, FAKE, FAKE, FAKE, ALIGNED_WS, need - 1, None) == I.SV_ERR_WORKSPACE
+    assert lib.spec_verify_greedy(FAKE, 0, 4, 2, 100, FAKE, FAKE, FAKE, ctypes.c_void_p(0x10010), need, None) == I.SV_ERR_WORKSPACE
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert lib.spec_verify_greedy(FAKE, 0, 0, 3, 100, FAKE, FAKE, FAKE, ALIGNED_WS, 256, None) == binding.SV_OK
+    assert lib.spec_last_launch_count() == 0
+
+
+def test_profile_hook_arguments(lib):
+    assert lib.spec_profile_set_events(FAKE, None) == binding.SV_ERR_INVALID
+    assert lib.spec_profile_set_events(None, None) == binding.SV_OK
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "lib_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        binding.load()

@@ -1,0 +1,303 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+identical seeded inputs, at the full workload sizes and at small shapes that
+span several chunks/tiles with ragged tails, plus the edge cases."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_verification_11_gb300 import api, binding as B_, workloads as W
+
+from paritylib import compare_greedy, compare_sampling, record
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle(batch, temperature=None):
+    T = batch.temperature if temperature is None else temperature
+    greedy = T == 0
+    return oracle.verify(batch.logits, batch.q, batch.draft, batch.uniforms, batch.row_offsets,
+                         T if not greedy else 1.0, greedy=greedy)
+
+
+def _gpu_fixed(batch, dev, diag=True):
+    logits = batch.logits.to(dev)
+    draft = batch.draft.to(dev)
+    if batch.temperature == 0:
+        out, al = api.verify_greedy(logits, draft, batch.K)
+        torch.cuda.synchronize()
+        return out.cpu().numpy(), al.cpu().numpy(), None
+    out, al, dg = api.verify_sample(logits, batch.q.to(dev), draft, batch.uniforms.to(dev), batch.K,
+                                    batch.temperature, diag=diag)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), al.cpu().numpy(), (dg.cpu().numpy() if dg is not None else None)
+
+
+def _gpu_ragged(batch, dev, T=None, diag=True):
+    T = batch.temperature if T is None else T
+    q = batch.q.to(dev) if batch.q is not None else None
+    u = batch.uniforms.to(dev) if batch.uniforms is not None else None
+    out, al, dg = api.verify_ragged(batch.logits.to(dev), q, batch.row_offsets.to(dev),
+                                    batch.draft.to(dev), u, T, diag=diag and T > 0)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), al.cpu().numpy(), (dg.cpu().numpy() if dg is not None else None)
+
+
+def _status(dev):
+    ws = api._default_ws[(str(dev), torch.cuda.current_stream(dev).cuda_stream)].buf
+    return B_.spec_verify_last_device_status(ws)
+
+
+# --------------------------------------------------------------------------
+# the five workloads at full size
+# --------------------------------------------------------------------------
+def test_greedy_workload_bit_exact(cuda_device):
+    b = W.greedy()
+    out, al, _ = _gpu_fixed(b, cuda_device)
+    compare_greedy("greedy B=32 K=5 V=32000 bf16", b.row_offsets, out, al, _oracle(b))
+    assert _status(cuda_device) == (B_.SV_OK, 0)
+
+
+def test_tiny_workload_batched(cuda_device):
+    b = W.tiny()
+    out, al, dg = _gpu_fixed(b, cuda_device)
+    compare_sampling("tiny B=1x1000 K=4 V=1024", b.row_offsets, out, al, dg, _oracle(b))
+
+
+def test_tiny_workload_as_single_calls(cuda_device):
+    """The 1000 independent steps as B=1 calls give the batched results."""
+    b = W.tiny()
+    dev = cuda_device
+    logits, q, x, u = b.logits.to(dev), b.q.to(dev), b.draft.to(dev), b.uniforms.to(dev)
+    outs, als = [], []
+    for s in range(100):
+        o, a, _ = api.verify_sample(logits[5 * s:5 * s + 5], q[4 * s:4 * s + 4], x[4 * s:4 * s + 4],
+                                    u[5 * s:5 * s + 5], 4, 1.0)
+        outs.append(o)
+        als.append(a)
+    torch.cuda.synchronize()
+    o_all, a_all, _ = api.verify_sample(logits[:500], q[:400], x[:400], u[:500], 4, 1.0)
+    assert torch.equal(torch.cat(outs), o_all) and torch.equal(torch.cat(als), a_all)
+
+
+def test_sampling_workload_full(cuda_device):
+    b = W.sampling()
+    out, al, dg = _gpu_fixed(b, cuda_device)
+    compare_sampling("sampling B=64 K=4 V=128256 T=0.7", b.row_offsets, out, al, dg, _oracle(b))
+    st, flags = _status(cuda_device)
+    assert st == B_.SV_OK and flags & ~B_.SV_FLAG_ZERO_RESIDUAL == 0
+
+
+@pytest.fixture(scope="module")
+def ragged_batch():
+    return W.ragged()
+
+
+def test_ragged_workload_full(cuda_device, ragged_batch):
+    b = ragged_batch
+    out, al, dg = _gpu_ragged(b, cuda_device)
+    compare_sampling("ragged B=256 K_i~U{0..8} V=151936", b.row_offsets, out, al, dg, _oracle(b))
+
+
+def test_ragged_workload_greedy(cuda_device, ragged_batch):
+    b = ragged_batch
+    out, al, _ = _gpu_ragged(b, cuda_device, T=0.0)
+    compare_greedy("ragged greedy B=256 V=151936", b.row_offsets, out, al, _oracle(b, temperature=0.0))
+
+
+# --------------------------------------------------------------------------
+# shapes: several chunks / tiles, ragged tails, vector and scalar paths
+# --------------------------------------------------------------------------
+def _rand_batch(seed, B, K, V, dtype, T, sigma=2.0, noise=1.0, ties=False):
+    g = torch.Generator().manual_seed(seed)
+    R = B * (K + 1)
+    z = torch.randn(R, V, generator=g) * sigma
+    if ties:
+        z = torch.round(z * 2) / 2
+    z = z.to(dtype)
+    ro = W.fixed_offsets(B, K)
+    if T == 0:
+        idx = W._draft_rows_index(ro)
+        noisy = z[idx].float() + torch.randn(len(idx), V, generator=g) * noise
+        x = torch.argmax(noisy, 1).to(torch.int32)
+        return W.Batch("rand", z, None, x, None, ro, B, K, V, 0.0)
+    idx = W._draft_rows_index(ro)
+    q = W._softmax_rows_f32(z[idx].float() + torch.randn(len(idx), V, generator=g) * noise, T)
+    x = W._draw_from(q, g) if len(idx) else torch.empty(0, dtype=torch.int32)
+    u = torch.from_numpy(W.philox_uniforms(seed, R))
+    return W.Batch("rand", z, q, x, u, ro, B, K, V, T)
+
+
+GREEDY_SHAPES = [(1, 3), (7, 2), (1000, 5), (8191, 1), (8192, 4), (16385, 3), (40001, 2), (65536, 0)]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("V,K", GREEDY_SHAPES)
+def test_greedy_shapes_with_ties(cuda_device, dtype, V, K):
+    b = _rand_batch(10 + V + K, B=9, K=K, V=V, dtype=dtype, T=0.0, ties=True)
+    out, al, _ = _gpu_fixed(b, cuda_device)
+    compare_greedy(f"greedy V={V} K={K} {dtype}", b.row_offsets, out, al, _oracle(b))
+
+
+SAMPLE_SHAPES = [(5, 2, 1.0), (1000, 4, 0.7), (4097, 3, 1.3), (8192, 4, 1.0), (10007, 5, 0.9),
+                 (25000, 7, 1.0), (70001, 2, 0.5), (131072, 1, 1.0)]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("V,K,T", SAMPLE_SHAPES)
+def test_sampling_shapes(cuda_device, dtype, V, K, T):
+    b = _rand_batch(100 + V + K, B=24, K=K, V=V, dtype=dtype, T=T)
+    out, al, dg = _gpu_fixed(b, cuda_device)
+    compare_sampling(f"sample V={V} K={K} T={T} {dtype}", b.row_offsets, out, al, dg, _oracle(b))
+
+
+def test_sampling_k_zero_is_bonus_only(cuda_device):
+    b = _rand_batch(5, B=40, K=0, V=3000, dtype=torch.float32, T=1.0)
+    out, al, dg = _gpu_fixed(b, cuda_device)
+    assert np.all(al == 1)
+    compare_sampling("sample K=0", b.row_offsets, out, al, dg, _oracle(b))
+
+
+def test_ragged_small_mixed(cuda_device):
+    g = torch.Generator().manual_seed(77)
+    ks = [0, 3, 0, 8, 1, 255, 2]
+    b = W.make_sampling_batch("r", 77, B=len(ks), K=None, V=3001, T=0.8, logit_sigma=2.0,
+                              noise_sigma=0.7, k_list=ks)
+    out, al, dg = _gpu_ragged(b, cuda_device)
+    compare_sampling("ragged small incl. K=255", b.row_offsets, out, al, dg, _oracle(b))
+
+
+# --------------------------------------------------------------------------
+# special cases and errors
+# --------------------------------------------------------------------------
+def test_q_equals_p_accepts_everything(cuda_device):
+    B, K, V, T = 64, 4, 5000, 0.9
+    g = torch.Generator().manual_seed(8)
+    z = torch.randn(B * (K + 1), V, generator=g) * 2
+    ro = W.fixed_offsets(B, K)
+    idx = W._draft_rows_index(ro)
+    q = W._softmax_rows_f32(z[idx], T)
+    x = W._draw_from(q, g)
+    u = torch.from_numpy(W.philox_uniforms(8, B * (K + 1)))
+    b = W.Batch("qp", z, q, x, u, ro, B, K, V, T)
+    out, al, dg = _gpu_fixed(b, cuda_device)
+    orc = _oracle(b)
+    full = al == K + 1
+    assert np.all(full | (orc["near_tie_accept"] > 0))
+    compare_sampling("q == p", b.row_offsets, out, al, dg, orc)
+
+
+def test_invalid_draft_id_is_isolated(cuda_device):
+    b = _rand_batch(3, B=6, K=3, V=2000, dtype=torch.float32, T=1.0)
+    x = b.draft.clone()
+    x[5] = 2000  # request 1, position 2
+    x[13] = -4   # request 4, position 1
+    b.draft = x
+    out, al, dg = _gpu_fixed(b, cuda_device)
+    orc = _oracle(b)
+    assert orc["invalid"] == 2
+    assert al[1] == 0 and al[4] == 0 and np.all(out[4:8] == -1) and np.all(out[16:20] == -1)
+    st, flags = _status(cuda_device)
+    assert st == B_.SV_ERR_DEVICE_INPUT and flags & B_.SV_FLAG_BAD_TOKEN
+    keep = [0, 2, 3, 5]
+    assert np.array_equal(al[keep], orc["accept_len"][keep])
+    # the status word was cleared by the read
+    assert _status(cuda_device) == (B_.SV_OK, 0)
+
+
+def test_malformed_offsets_invalidate_call(cuda_device):
+    dev = cuda_device
+    V = 500
+    z = torch.randn(10, V, device=dev)
+    q = torch.full((7, V), 1.0 / V, device=dev)
+    x = torch.zeros(7, dtype=torch.int32, device=dev)
+    u = torch.full((10,), 0.5, device=dev)
+    for bad in ([0, 4, 3, 10], [1, 4, 7, 10], [0, 4, 7, 9]):
+        ro = torch.tensor(bad, dtype=torch.int32, device=dev)
+        out, al, _ = api.verify_ragged(z, q, ro, x, u, 1.0)
+        torch.cuda.synchronize()
+        assert torch.all(al == 0) and torch.all(out == -1)
+        st, flags = _status(dev)
+        assert st == B_.SV_ERR_DEVICE_INPUT and flags & B_.SV_FLAG_BAD_OFFSETS
+    # a good call right after works (workspace left reusable)
+    ro = torch.tensor([0, 4, 7, 10], dtype=torch.int32, device=dev)
+    out, al, _ = api.verify_ragged(z, q, ro, x, u, 1.0)
+    torch.cuda.synchronize()
+    assert torch.all(al >= 1)
+
+
+def test_zero_residual_falls_back_to_p(cuda_device):
+    dev = cuda_device
+    z = torch.log(torch.tensor([[0.5, 0.5], [0.5, 0.5]])).to(dev)
+    q = torch.tensor([[0.6, 0.6]], device=dev)
+    x = torch.tensor([0], dtype=torch.int32, device=dev)
+    u = torch.tensor([0.99, 0.75], device=dev)
+    out, al, _ = api.verify_sample(z, q, x, u, 1, 1.0)
+    torch.cuda.synchronize()
+    assert al.item() == 1 and out[0].item() == 1
+    st, flags = _status(dev)
+    assert st == B_.SV_OK and flags & B_.SV_FLAG_ZERO_RESIDUAL
+
+
+def test_empty_batch(cuda_device):
+    dev = cuda_device
+    z = torch.empty(0, 100, device=dev)
+    out, al = api.verify_greedy(z, torch.empty(0, dtype=torch.int32, device=dev), 3)
+    assert out.numel() == 0 and al.numel() == 0
+
+
+def test_repeat_calls_identical_and_canaries(cuda_device):
+    dev = cuda_device
+    b = _rand_batch(21, B=16, K=4, V=9000, dtype=torch.float32, T=1.0)
+    logits, q, x, u = b.logits.to(dev), b.q.to(dev), b.draft.to(dev), b.uniforms.to(dev)
+    R, Bn = b.rows, b.B
+    sentinel = -777
+    out_buf = torch.full((R + 64,), sentinel, dtype=torch.int32, device=dev)
+    al_buf = torch.full((Bn + 64,), sentinel, dtype=torch.int32, device=dev)
+    dg_buf = torch.full((R + Bn + 64,), 12345.0, device=dev)
+    ws = B_.workspace(B_.spec_verify_workspace_size(Bn, R, b.V) + 4096, dev)
+    ws_guard = ws[-4096:]
+    ws_guard.fill_(0xA5)
+    results = []
+    for _ in range(3):
+        B_.spec_verify_sample(logits, q, Bn, 4, b.V, 1.0, x, u, out_buf[32:32 + R], al_buf[32:32 + Bn],
+                              ws[:-4096], diag=dg_buf[32:32 + R + Bn])
+        torch.cuda.synchronize()
+        results.append((out_buf.clone(), al_buf.clone()))
+    for o, a in results[1:]:
+        assert torch.equal(o, results[0][0]) and torch.equal(a, results[0][1])
+    assert torch.all(out_buf[:32] == sentinel) and torch.all(out_buf[32 + R:] == sentinel)
+    assert torch.all(al_buf[:32] == sentinel) and torch.all(al_buf[32 + Bn:] == sentinel)
+    assert torch.all(dg_buf[:32] == 12345.0) and torch.all(dg_buf[32 + R + Bn:] == 12345.0)
+    assert torch.all(ws_guard == 0xA5)
+
+
+# --------------------------------------------------------------------------
+# the emitted token's law on the GPU (10^6 trials, V = 16)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("variant", ["near", "onehot", "zeros", "far"])
+def test_emitted_token_law_chisquare_gpu(cuda_device, variant):
+    from test_oracle_pins import _chisq_pvalue, _q_variants
+    rng = np.random.default_rng(321)
+    V, K, T, n = 16, 2, 1.0, 1_000_000
+    z = rng.normal(0, 1.0, size=(K + 1, V))
+    q = _q_variants(z, rng)[variant]
+    draft = np.stack([rng.choice(V, size=n, p=q[j].astype(np.float64) / q[j].astype(np.float64).sum())
+                      for j in range(K)], axis=1).astype(np.int32).reshape(-1)
+    uni = torch.from_numpy(W.philox_uniforms(4242, n * (K + 1)))
+    dev = cuda_device
+    logits = torch.from_numpy(z.astype(np.float32)).to(dev).repeat(n, 1)
+    qq = torch.from_numpy(q).to(dev).repeat(n, 1)
+    out, al, _ = api.verify_sample(logits, qq, torch.from_numpy(draft).to(dev), uni.to(dev), K, T)
+    out = out.view(n, K + 1).cpu().numpy()
+    al = al.cpu().numpy()
+    p = oracle.softmax_rows(z.astype(np.float32), T)
+    pv = []
+    for j in range(K + 1):
+        sel = al > j
+        counts = np.bincount(out[sel, j], minlength=V).astype(np.float64)
+        pv.append(_chisq_pvalue(counts, p[j]))
+    record(f"chi-square GPU {variant}", {"pvalues": pv, "trials": n, "mean_al": float(al.mean())})
+    assert min(pv) > 1e-3
