@@ -216,6 +216,10 @@ def run_ours(args):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
+    for evs in ev:  # torch creates an event on its first record; the library re-records them
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
     clocks = Clocks(local)
     launches = 0
     if world > 1:

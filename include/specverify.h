@@ -40,7 +40,9 @@
  *   - Input errors only the device can see (a drafted id outside [0, V),
  *     malformed CSR offsets) set bits of a status word kept in the workspace;
  *     the affected request gets AL = 0 and all its output slots -1, the others
- *     are unaffected.  spec_verify_last_device_status() reads and clears it.
+ *     are unaffected (malformed CSR offsets invalidate every request of the
+ *     call).  The word accumulates over calls until
+ *     spec_verify_last_device_status() reads and clears it.
  *     No kernel traps.
  *   - Layout of a request b with K_b drafts and first logits row r_b:
  *       logits rows r_b .. r_b + K_b            (position j = row r_b + j)
@@ -49,8 +51,10 @@
  *                                                u_{K_b} the final draw)
  *     Fixed-K calls use r_b = b (K+1).  Output slots past AL hold -1.
  *   - A workspace may not be shared by calls that overlap on the device.
- *     It needs no initialisation: every call leaves it reusable, even one
- *     that reported a device input error.
+ *     Zero-fill it once before its first use (cudaMemsetAsync).  After that
+ *     it serves calls of any shape in turn: every call that completes leaves
+ *     its per-request counters at zero (a call that reported SV_ERR_TIMEOUT
+ *     may not: zero-fill the workspace again after one).
  *   - `diag` (may be NULL) receives per-token diagnostics in fp32:
  *       diag[i], i < Nq = rows - B : p_j(x_j) of draft slot i
  *       diag[Nq + 2b]              : mass R of the distribution the final
@@ -161,8 +165,9 @@ sv_status spec_lmhead_verify(const void *hidden, const void *w_vocab_t, int d, c
                              float *diag, void *ws, size_t ws_bytes, void *stream);
 
 /*
- * Synchronises `stream`, returns the device status word of workspace `ws`
- * in *flags (SV_FLAG_* bits, may be NULL) and clears it.  Returns
+ * Synchronises `stream` and returns in *flags (SV_FLAG_* bits, may be NULL)
+ * the device status word of workspace `ws` (the OR of every call since the
+ * last read), then clears it.  Returns
  * SV_ERR_DEVICE_INPUT if an input-error bit was set, SV_ERR_TIMEOUT if the
  * timeout bit was set, SV_ERR_CUDA on a CUDA error, else SV_OK.
  */

@@ -11,7 +11,6 @@ constexpr int kThreads = 256;          // every verification kernel runs 8 warps
 constexpr int kWarps = kThreads / 32;
 constexpr int kLoadsPerThread = 8;     // 16-byte loads in flight per thread per chunk
 constexpr int kTileElems = kThreads * 4;  // residual tile: 4 tokens per thread
-constexpr int kTilesPerPart = 8;          // residual CTA covers 8 tiles
 constexpr int kMaxRowsPerRequest = 256;   // SV_MAX_K + 1
 
 // Elements per 16-byte vector and per stats chunk for each logits type.
@@ -99,20 +98,109 @@ __device__ __forceinline__ void warp_am_reduce(float &v, int &i) {
     }
 }
 
-// Epoch ticket: the high word holds the call's epoch, the low word the number
-// of CTAs of this call that arrived.  A stale word from an earlier call
-// (epoch differs) restarts at one, so the workspace never needs clearing.
-// Lock-free: every failed CAS means another CTA's update went through.
-__device__ __forceinline__ uint32_t ticket_arrive(unsigned long long *t, uint32_t epoch) {
-    unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(t);
-    while (true) {
-        const unsigned long long nxt = (static_cast<uint32_t>(cur >> 32) == epoch)
-                                           ? cur + 1ull
-                                           : ((static_cast<unsigned long long>(epoch) << 32) | 1ull);
-        const unsigned long long prev = atomicCAS(t, cur, nxt);
-        if (prev == cur) return static_cast<uint32_t>(nxt & 0xffffffffull);
-        cur = prev;
-    }
+}  // namespace sv
+
+namespace sv {
+
+// ---------------------------------------------------------------------------
+// mbarrier / bulk-copy primitives (inline PTX, sm_90+ forms valid on sm_103a)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                     smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: gives up after `budget` SM clock cycles and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, long long budget) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > budget) return false;
+    }
+    return true;
+}
+
+// Global -> shared bulk copy completing on an mbarrier (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Release / acquire helpers for the per-request tickets.
+__device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+}  // namespace sv
+
+namespace sv {
+
+// ---------------------------------------------------------------------------
+// Thread-block cluster primitives
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Whole-cluster barrier; release/acquire orders shared-memory writes before it
+// with distributed-shared-memory reads after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Read a float from the shared memory of CTA `rank` of this cluster at the
+// address that `p` has in this CTA.
+__device__ __forceinline__ float ld_dsmem_f32(const float *p, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(p)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+}  // namespace sv
+
+namespace sv {
+// Programmatic dependent launch: let the next kernel in the stream be
+// scheduled early / wait for the previous kernel's completion and memory.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 }  // namespace sv

@@ -5,7 +5,7 @@
 #include <stdint.h>
 
 namespace sv {
-uint32_t next_epoch();             // unique tag of one call (tickets compare it)
+int sm_count();                    // SMs of the current device
 void prof_begin(cudaStream_t s);   // profiling hook around the dominant kernel
 void prof_end(cudaStream_t s);
 void set_launches(int n);          // kernels launched by the last call (this thread)

@@ -1,28 +1,28 @@
 // Verification kernels and the C ABI of libspecverify.so (sm_103a).
 //
-// Pass 1  stats_decide_kernel   one CTA per (logits row, chunk of the vocabulary)
-//         streams the logits once with 128-bit loads and reduces the chunk to
+// Pass 1  stats_tma_kernel (rows 16-byte aligned) / stats_scalar_kernel (any)
+//         streams every logit once and reduces each 32 KB chunk of a row to
 //         (M, s) = (max z c, sum 2^(z c - M)) with c = log2(e)/T (sampling) or
-//         to (max z, first argmax) (greedy).  The last CTA of each request
-//         (epoch ticket) merges its rows' chunk partials and runs the decide
-//         step: accept tests u q(x) <= p(x), first-rejection scan, emitted
-//         drafts, AL, and the record of the row the final token comes from.
-// Pass 2  residual_kernel       (sampling only) one CTA per (request, 8 tiles
-//         of 1024 tokens) of the selected row: r = max(0, p - q) at a
-//         rejection or r = p for the bonus, tile masses; the last CTA of the
-//         request takes the prefix over tiles in fp64, finds the tile holding
-//         u R, and resolves the token inside it with a block scan that is
-//         bit-identical to the one that produced the tile's mass.
+//         to (max z, first argmax) (greedy).  The TMA variant is persistent:
+//         one CTA per SM, a producer warp feeding a 6-stage shared ring with
+//         bulk async copies, 8 consumer warps that need no block barrier.
+//         The arrival that completes a request's count (release atomic) runs
+//         the decide step in one warp: accept tests u q(x) <= p(x), ballot
+//         for the first rejection, emitted drafts, AL, and the record of the
+//         row the final token comes from.
+// Pass 2  residual_kernel (sampling only) one 2-CTA cluster per request over
+//         the selected row, one warp per 1024-token tile: r = max(0, p - q)
+//         at a rejection or r = p for the bonus, tile masses in shared
+//         memory; rank 0 takes the prefix over tiles in fp64 through
+//         distributed shared memory, finds the tile holding u R, and resolves
+//         the token inside it with the same warp scan that produced the
+//         tile's mass.
 //
 // The operation is the one stated on "Speculative Decoding in Large Language
 // Models", section 2 "Modified Rejection Sampling" (accept test, residual
 // p'(x)), with the stop at the first mismatch and the extra target token of
 // "Co-Designing AI Models Using Speculative Decoding", "What is speculative
 // decoding?".  See include/specverify.h for the full contract.
-#include <unistd.h>
-
-#include <atomic>
-#include <chrono>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -56,23 +56,23 @@ struct Args {
     int32_t *out_tokens;
     int32_t *accept_len;
     float *diag;
-    int B, K, V, rows, n_chunks, n_tiles, n_parts, n_draft;
+    int B, K, V, rows, n_chunks, n_tiles, n_draft;
     float c;  // log2(e) / T
-    uint32_t epoch;
     // workspace
     uint32_t *status;
     const int *csr_ok;
-    unsigned long long *tickets1;
-    unsigned long long *tickets2;
+    uint32_t *tickets1;
     Decision *dec;
     float2 *partials;
     float *tile_mass;
 };
 
+constexpr long long kWaitBudget = 4000000000ll;  // SM cycles (~2 s) before a wait gives up
+
 __device__ __forceinline__ void request_rows(const Args &a, int b, int &r0, int &nr) {
     if (a.row_offsets) {
-        r0 = a.row_offsets[b];
-        nr = a.row_offsets[b + 1] - r0;
+        r0 = __ldg(a.row_offsets + b);
+        nr = __ldg(a.row_offsets + b + 1) - r0;
     } else {
         r0 = b * (a.K + 1);
         nr = a.K + 1;
@@ -95,99 +95,138 @@ __device__ __forceinline__ float logit_at(const Args &a, size_t i) {
     return Elem<T>::at(reinterpret_cast<const T *>(a.logits), i);
 }
 
-// ---------------------------------------------------------------------------
-// Decide step of request b (whole CTA).  Runs after every chunk partial of the
-// request's rows is visible.
-// ---------------------------------------------------------------------------
-struct DecideSmem {
-    float M[kMaxRowsPerRequest];
-    float S[kMaxRowsPerRequest];
-    int arg[kMaxRowsPerRequest];
-    int bad;
-    int kstar;
-};
+template <bool kSample>
+__device__ __forceinline__ void warp_partial_reduce(float &ra, int &rb) {
+    if (kSample) {
+        float s = __int_as_float(rb);
+        warp_ms_reduce(ra, s);
+        rb = __float_as_int(s);
+    } else {
+        warp_am_reduce(ra, rb);
+    }
+}
 
+template <bool kSample>
+__device__ __forceinline__ void merge_pair(float &ra, int &rb, float2 w) {
+    if (kSample) {
+        float s = __int_as_float(rb);
+        ms_merge(ra, s, w.x, w.y);
+        rb = __float_as_int(s);
+    } else {
+        am_merge(ra, rb, w.x, __float_as_int(w.y));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Decide step of request b, run by one warp once every chunk partial of the
+// request's rows is visible.  Lane j owns row jb + j: it merges the row's
+// chunk partials in chunk order, evaluates the accept test of its draft, and
+// a ballot finds the first rejection.
+// ---------------------------------------------------------------------------
 template <typename T, bool kSample>
-__device__ void decide(const Args &a, int b, DecideSmem &sh) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__device__ void decide_warp(const Args &a, int b, int lane) {
     int r0, nr;
     request_rows(a, b, r0, nr);
     const int Kb = nr - 1;
     const int d0 = r0 - b;
-    if (tid == 0) {
-        sh.bad = 0;
-        sh.kstar = Kb;
+    if (lane == 0) a.tickets1[b] = 0u;  // every arrival of this call is in: leave the counter clean
+    bool bad = false;
+    for (int j = lane; j < Kb; j += 32) {
+        const int x = __ldg(a.draft + d0 + j);
+        bad |= (x < 0 || x >= a.V);
     }
-    __syncthreads();
-    for (int j = tid; j < Kb; j += kThreads) {
-        const int x = a.draft[d0 + j];
-        if (x < 0 || x >= a.V) sh.bad = 1;
-    }
-    __syncthreads();
-    if (sh.bad) {
-        for (int j = tid; j < nr; j += kThreads) a.out_tokens[r0 + j] = -1;
-        if (tid == 0) {
+    if (__any_sync(0xffffffffu, bad)) {
+        for (int j = lane; j < nr; j += 32) a.out_tokens[r0 + j] = -1;
+        if (lane == 0) {
             a.accept_len[b] = 0;
             if (kSample) {
                 Decision d{};
-                d.valid = 0;
                 a.dec[b] = d;
             }
             atomicOr(a.status, SV_FLAG_BAD_TOKEN);
         }
         return;
     }
-    // merge the chunk partials of every row of the request (one warp per row)
-    for (int j = warp; j < nr; j += kWarps) {
-        const float2 *P = a.partials + static_cast<size_t>(r0 + j) * a.n_chunks;
-        if (kSample) {
-            float M = -INFINITY, s = 0.f;
+    int ks = Kb;
+    float Msel = 0.f, Ssel = 1.f;
+    int argsel = 0;
+    for (int jb = 0; jb < nr; jb += 32) {
+        const int j = jb + lane;
+        // gathers of this block's drafts first: their latency overlaps the merges
+        int x = 0;
+        float z = 0.f, qv = 0.f, u = 0.f;
+        if (j < Kb) {
+            x = __ldg(a.draft + d0 + j);
+            if (kSample) {
+                z = logit_at<T>(a, static_cast<size_t>(r0 + j) * a.V + x);
+                qv = __ldg(a.q + static_cast<size_t>(d0 + j) * a.V + x);
+                u = __ldg(a.uniforms + r0 + j);
+            }
+        }
+        // merge the chunk partials of rows jb .. jb+31: lanes over chunks, all
+        // loads of a row issued together, butterfly across lanes
+        float M = -INFINITY, S = 0.f, bv = -INFINITY;
+        int bi = 0x7fffffff;
+        const int rows_here = min(32, nr - jb);
+        for (int rg = 0; rg < rows_here; rg += 8) {
+            float ma[8];
+            int mb[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                ma[i] = -INFINITY;
+                mb[i] = kSample ? __float_as_int(0.f) : 0x7fffffff;
+            }
             for (int c = lane; c < a.n_chunks; c += 32) {
-                const float2 v = __ldcg(P + c);
-                ms_merge(M, s, v.x, v.y);
+                float2 w[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)  // 8 rows' loads in flight together
+                    w[i] = (rg + i < rows_here)
+                               ? __ldcg(a.partials + static_cast<size_t>(r0 + jb + rg + i) * a.n_chunks + c)
+                               : make_float2(-INFINITY, kSample ? 0.f : __int_as_float(0x7fffffff));
+#pragma unroll
+                for (int i = 0; i < 8; ++i) merge_pair<kSample>(ma[i], mb[i], w[i]);
             }
-            warp_ms_reduce(M, s);
-            if (lane == 0) {
-                sh.M[j] = M;
-                sh.S[j] = s;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                warp_partial_reduce<kSample>(ma[i], mb[i]);
+                if (lane == rg + i) {
+                    if (kSample) {
+                        M = ma[i];
+                        S = __int_as_float(mb[i]);
+                    } else {
+                        bv = ma[i];
+                        bi = mb[i];
+                    }
+                }
             }
-        } else {
-            float v = -INFINITY;
-            int i = 0x7fffffff;
-            for (int c = lane; c < a.n_chunks; c += 32) {
-                const float2 w = __ldcg(P + c);
-                am_merge(v, i, w.x, __float_as_int(w.y));
+        }
+        bool rej = false;
+        if (j < Kb) {
+            if (kSample) {
+                const float p = exp2f(fmaf(z, a.c, -M)) / S;
+                rej = !(u * qv <= p);
+                if (a.diag) a.diag[d0 + j] = p;
+            } else {
+                rej = (x != bi);
             }
-            warp_am_reduce(v, i);
-            if (lane == 0) sh.arg[j] = i;
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, rej);
+        if (m || jb + 32 >= nr) {
+            const int src = m ? (__ffs(m) - 1) : (Kb - jb);
+            ks = jb + src;
+            Msel = __shfl_sync(0xffffffffu, M, src);
+            Ssel = __shfl_sync(0xffffffffu, S, src);
+            argsel = __shfl_sync(0xffffffffu, bi, src);
+            break;
         }
     }
-    __syncthreads();
-    // accept tests at every drafted position; k* = the first rejection
-    for (int j = tid; j < Kb; j += kThreads) {
-        const int x = a.draft[d0 + j];
-        bool acc;
-        if (kSample) {
-            const float z = logit_at<T>(a, static_cast<size_t>(r0 + j) * a.V + x);
-            const float p = exp2f(fmaf(z, a.c, -sh.M[j])) / sh.S[j];
-            const float qv = __ldg(a.q + static_cast<size_t>(d0 + j) * a.V + x);
-            const float u = __ldg(a.uniforms + r0 + j);
-            acc = (u * qv <= p);
-            if (a.diag) a.diag[d0 + j] = p;
-        } else {
-            acc = (x == sh.arg[j]);
-        }
-        if (!acc) atomicMin(&sh.kstar, j);
-    }
-    __syncthreads();
-    const int ks = sh.kstar;
-    for (int j = tid; j < nr; j += kThreads) {
+    for (int j = lane; j < nr; j += 32) {
         int v = -1;
-        if (j < ks) v = a.draft[d0 + j];
-        else if (j == ks && !kSample) v = sh.arg[j];
+        if (j < ks) v = __ldg(a.draft + d0 + j);
+        else if (j == ks && !kSample) v = argsel;
         a.out_tokens[r0 + j] = v;
     }
-    if (tid == 0) {
+    if (lane == 0) {
         a.accept_len[b] = ks + 1;
         if (kSample) {
             Decision d;
@@ -195,8 +234,8 @@ __device__ void decide(const Args &a, int b, DecideSmem &sh) {
             d.qrow = (ks < Kb) ? d0 + ks : -1;
             d.slot = r0 + ks;
             d.valid = 1;
-            d.M = sh.M[ks];
-            d.invS = 1.f / sh.S[ks];
+            d.M = Msel;
+            d.invS = 1.f / Ssel;
             d.u = __ldg(a.uniforms + r0 + Kb);
             d.pad = 0;
             a.dec[b] = d;
@@ -204,365 +243,709 @@ __device__ void decide(const Args &a, int b, DecideSmem &sh) {
     }
 }
 
-// ---------------------------------------------------------------------------
-// Pass 1: per-(row, chunk) statistics + decide by the request's last CTA
-// ---------------------------------------------------------------------------
-template <typename T, bool kSample, bool kVecPath>
-__global__ void __launch_bounds__(kThreads) stats_decide_kernel(Args a) {
-    constexpr int VEC = Elem<T>::kVec;
-    constexpr int CHUNK = chunk_elems<T>();
-    __shared__ float red_a[kWarps];
-    __shared__ int red_b[kWarps];
-    __shared__ int s_last;
-    __shared__ DecideSmem sh;
-
-    if (a.csr_ok && !__ldcg(a.csr_ok)) return;
-    const int tid = threadIdx.x;
-    const int item = blockIdx.x;
-    const int row = item / a.n_chunks;
-    const int chunk = item - row * a.n_chunks;
-    const int c0 = chunk * CHUNK;
-    const int n = min(CHUNK, a.V - c0);
-    const T *zrow = reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(row) * a.V + c0;
-
-    // element (i, k) of this thread is token c0 + (i * kThreads + tid) * VEC + k
-    float vals[kLoadsPerThread][VEC];
-    if (kVecPath) {
-        uint4 raw[kLoadsPerThread];
-#pragma unroll
-        for (int i = 0; i < kLoadsPerThread; ++i) {
-            const int e = (i * kThreads + tid) * VEC;
-            if (e < n) raw[i] = ld_stream_u4(zrow + e);
-            else raw[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int i = 0; i < kLoadsPerThread; ++i) unpack(raw[i], vals[i]);
-    } else {
-#pragma unroll
-        for (int i = 0; i < kLoadsPerThread; ++i)
-#pragma unroll
-            for (int k = 0; k < VEC; ++k) {
-                const int e = (i * kThreads + tid) * VEC + k;
-                vals[i][k] = (e < n) ? Elem<T>::at(zrow, e) : 0.f;
-            }
-    }
-
-    float ra = 0.f;
-    int rb = 0;
+// Reduce `vals` (this lane's elements, element (j, k) valid when idx(j,k) < n)
+// to the lane's partial: sampling (M, s) or greedy (max, first index).
+template <bool kSample, int VEC>
+__device__ __forceinline__ void lane_partial(const float (&vals)[kLoadsPerThread][VEC], const int (&e0)[kLoadsPerThread],
+                                             int n, int c0, float c, float &ra, int &rb) {
     if (kSample) {
         float bm = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < kLoadsPerThread; ++i)
+        for (int j = 0; j < kLoadsPerThread; ++j)
 #pragma unroll
             for (int k = 0; k < VEC; ++k)
-                if ((i * kThreads + tid) * VEC + k < n) bm = fmaxf(bm, vals[i][k]);
-        const float M = bm * a.c;
+                if (e0[j] + k < n) bm = fmaxf(bm, vals[j][k]);
+        const float M = bm * c;
         float s = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
-            for (int i = 0; i < kLoadsPerThread; ++i)
+            for (int j = 0; j < kLoadsPerThread; ++j)
 #pragma unroll
                 for (int k = 0; k < VEC; ++k)
-                    if ((i * kThreads + tid) * VEC + k < n) s += ex2(fmaf(vals[i][k], a.c, -M));
+                    if (e0[j] + k < n) s += ex2(fmaf(vals[j][k], c, -M));
         }
-        float Mw = M, sw = s;
-        warp_ms_reduce(Mw, sw);
-        if ((tid & 31) == 0) {
-            red_a[tid >> 5] = Mw;
-            red_b[tid >> 5] = __float_as_int(sw);
-        }
-        __syncthreads();
-        if (tid < 32) {
-            float Mx = (tid < kWarps) ? red_a[tid] : -INFINITY;
-            float sx = (tid < kWarps) ? __int_as_float(red_b[tid]) : 0.f;
-            warp_ms_reduce(Mx, sx);
-            ra = Mx;
-            rb = __float_as_int(sx);
-        }
+        ra = M;
+        rb = __float_as_int(s);
     } else {
         float bv = -INFINITY;
         int bi = 0x7fffffff;
 #pragma unroll
-        for (int i = 0; i < kLoadsPerThread; ++i)
+        for (int j = 0; j < kLoadsPerThread; ++j)
 #pragma unroll
-            for (int k = 0; k < VEC; ++k) {
-                const int e = (i * kThreads + tid) * VEC + k;
-                if (e < n && (bi == 0x7fffffff || vals[i][k] > bv)) {
-                    bv = vals[i][k];
-                    bi = c0 + e;
+            for (int k = 0; k < VEC; ++k)
+                if (e0[j] + k < n && (bi == 0x7fffffff || vals[j][k] > bv)) {
+                    bv = vals[j][k];
+                    bi = c0 + e0[j] + k;
                 }
-            }
-        warp_am_reduce(bv, bi);
-        if ((tid & 31) == 0) {
-            red_a[tid >> 5] = bv;
-            red_b[tid >> 5] = bi;
-        }
-        __syncthreads();
-        if (tid < 32) {
-            float vx = (tid < kWarps) ? red_a[tid] : -INFINITY;
-            int ix = (tid < kWarps) ? red_b[tid] : 0x7fffffff;
-            warp_am_reduce(vx, ix);
-            ra = vx;
-            rb = ix;
-        }
+        ra = bv;
+        rb = bi;
     }
-    if (tid == 0) {
+}
+
+
+
+// Publish the chunk partial of (row, chunk); the arrival that completes the
+// request's count runs the decide step.  Called by one whole warp.
+template <typename T, bool kSample>
+__device__ __forceinline__ void publish_partial(const Args &a, int row, int chunk, float ra, int rb, int lane) {
+    int islast = 0, b = 0;
+    if (lane == 0) {
         a.partials[static_cast<size_t>(row) * a.n_chunks + chunk] = make_float2(ra, __int_as_float(rb));
-        __threadfence();
-        const int b = request_of_row(a, row);
+        b = request_of_row(a, row);
         int r0, nr;
         request_rows(a, b, r0, nr);
-        const uint32_t cnt = ticket_arrive(a.tickets1 + b, a.epoch);
-        s_last = (cnt == static_cast<uint32_t>(nr) * static_cast<uint32_t>(a.n_chunks)) ? b : -1;
-        if (s_last >= 0) a.tickets1[b] = 0ull;  // every other CTA of the request has arrived
+        const uint32_t old = atom_add_release_gpu(a.tickets1 + b, 1u);
+        islast = (old + 1u == static_cast<uint32_t>(nr) * static_cast<uint32_t>(a.n_chunks));
+        if (islast) fence_acq_rel_gpu();
     }
-    __syncthreads();
-    if (s_last >= 0) {
-        __threadfence();
-        decide<T, kSample>(a, s_last, sh);
-    }
+    islast = __shfl_sync(0xffffffffu, islast, 0);
+    b = __shfl_sync(0xffffffffu, b, 0);
+    if (islast) decide_warp<T, kSample>(a, b, lane);
 }
 
 // ---------------------------------------------------------------------------
-// Pass 2: residual masses and the inverse-CDF draw
+// Pass 1, aligned rows: persistent CTA per SM over a contiguous range of
+// (row, chunk) items.
+//   warp 16 (producer)  streams 32 KB chunks with bulk async copies into a
+//                       kStages-deep shared ring (full/empty mbarriers);
+//   warps 0-15 (consumers) each reduce a 2 KB slice of every chunk into a
+//                       per-lane running partial of the current row segment;
+//                       at a row boundary each posts its warp partial to a
+//                       mailbox slot (mbarrier, 16 arrivals) and goes on;
+//   warp 17 (publisher) merges the 16 posts in warp order, writes the
+//                       segment's chunk partials, adds the segment's chunk
+//                       count to the request's counter (release atomic) and,
+//                       on the arrival that completes the count, runs the
+//                       decide step.
+// Consumers never wait on global memory or on each other.
 // ---------------------------------------------------------------------------
-struct ScanSmem {
-    float warp_tot[kWarps];
-    float tile_total;
-    int found_tile;
-    double found_base;
-    double R;
-    double t;
-    int vbest;
-    float rbest;
-    int zero_fallback;
+constexpr int kStages = 6;
+constexpr int kChunkBytes = 32768;
+constexpr int kConsumerWarps = 16;
+constexpr int kTmaVecs = kChunkBytes / 16 / (kConsumerWarps * 32);  // 16-byte vectors per lane per chunk
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kPublisherWarp = kConsumerWarps + 1;
+constexpr int kTmaThreads = (kConsumerWarps + 2) * 32;
+constexpr int kSegSlots = 4;
+
+struct SegMsg {
+    int row, first_chunk, n_chunk, pad;
 };
 
-// r(v) for the 4 tokens tile * 1024 + tid * 4 + k.  Same arithmetic (no
-// contraction) wherever it is called, so mass and search passes agree bitwise.
-template <typename T, bool kVecPath>
-__device__ __forceinline__ void tile_values(const T *zrow, const float *qrow, int V, int tile,
-                                            float c, float M, float invS, float (&r)[4]) {
-    const int e0 = tile * kTileElems + threadIdx.x * 4;
-    float z[4], qv[4] = {0.f, 0.f, 0.f, 0.f};
-    if (kVecPath && e0 + 4 <= V) {
-        if (sizeof(T) == 4) {
-            const float4 v = __ldg(reinterpret_cast<const float4 *>(zrow + e0));
-            z[0] = v.x; z[1] = v.y; z[2] = v.z; z[3] = v.w;
-        } else {
-            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(zrow + e0));
-            z[0] = __uint_as_float(v.x << 16);
-            z[1] = __uint_as_float(v.x & 0xffff0000u);
-            z[2] = __uint_as_float(v.y << 16);
-            z[3] = __uint_as_float(v.y & 0xffff0000u);
+struct TmaSmem {
+    alignas(128) unsigned char ring[kStages][kChunkBytes];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t seg_full[kSegSlots];
+    uint64_t seg_empty[kSegSlots];
+    float2 segpart[kSegSlots][kConsumerWarps];
+    SegMsg seg[kSegSlots];
+    int abort;
+};
+
+// Fold one chunk slice into the lane's running partial.  Vector j (VEC
+// consecutive tokens) is valid iff e0[j] < n (n is a multiple of VEC on this
+// path).  Max and sum run as trees over independent per-vector values.
+template <bool kSample, int NV, int VEC>
+__device__ __forceinline__ void lane_accumulate(const float (&vals)[NV][VEC], const int (&e0)[NV], int n, int c0,
+                                                float c, float &ra, int &rb) {
+    if (kSample) {
+        float vm[NV];
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            float m = vals[j][0];
+#pragma unroll
+            for (int k = 1; k < VEC; ++k) m = fmaxf(m, vals[j][k]);
+            vm[j] = (e0[j] < n) ? m : -INFINITY;
         }
-        if (qrow) {
-            const float4 w = __ldg(reinterpret_cast<const float4 *>(qrow + e0));
-            qv[0] = w.x; qv[1] = w.y; qv[2] = w.z; qv[3] = w.w;
+#pragma unroll
+        for (int w = 1; w < NV; w <<= 1)
+#pragma unroll
+            for (int j = 0; j + w < NV; j += 2 * w) vm[j] = fmaxf(vm[j], vm[j + w]);
+        const float bm = vm[0];
+        if (bm != -INFINITY) {
+            const float Mn = fmaxf(ra, bm * c);
+            float acc[NV];
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                float e[VEC];
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) e[k] = ex2(fmaf(vals[j][k], c, -Mn));
+#pragma unroll
+                for (int w = 1; w < VEC; w <<= 1)
+#pragma unroll
+                    for (int k = 0; k + w < VEC; k += 2 * w) e[k] += e[k + w];
+                acc[j] = (e0[j] < n) ? e[0] : 0.f;
+            }
+#pragma unroll
+            for (int w = 1; w < NV; w <<= 1)
+#pragma unroll
+                for (int j = 0; j + w < NV; j += 2 * w) acc[j] += acc[j + w];
+            const float s_old = __int_as_float(rb) * ex2(ra - Mn);  // ra = -inf: 0
+            ra = Mn;
+            rb = __float_as_int(s_old + acc[0]);
         }
     } else {
+        float vv[NV];
+        int vi[NV];
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            float m = vals[j][0];
+            int mi = 0;
+#pragma unroll
+            for (int k = 1; k < VEC; ++k)
+                if (vals[j][k] > m) {
+                    m = vals[j][k];
+                    mi = k;
+                }
+            vv[j] = (e0[j] < n) ? m : -INFINITY;
+            vi[j] = (e0[j] < n) ? c0 + e0[j] + mi : 0x7fffffff;
+        }
+#pragma unroll
+        for (int w = 1; w < NV; w <<= 1)
+#pragma unroll
+            for (int j = 0; j + w < NV; j += 2 * w) am_merge(vv[j], vi[j], vv[j + w], vi[j + w]);
+        if (vi[0] != 0x7fffffff) am_merge(ra, rb, vv[0], vi[0]);
+    }
+}
+
+template <bool kSample>
+__device__ __forceinline__ void partial_identity(float &ra, int &rb) {
+    ra = -INFINITY;
+    rb = kSample ? __float_as_int(0.f) : 0x7fffffff;
+}
+
+template <typename T, bool kSample>
+__global__ void __launch_bounds__(kTmaThreads, 1) stats_tma_kernel(Args a) {
+    constexpr int VEC = Elem<T>::kVec;
+    constexpr int CHUNK = chunk_elems<T>();
+    static_assert(CHUNK * sizeof(T) == kChunkBytes, "chunk must fill one ring stage");
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    TmaSmem &sm = *reinterpret_cast<TmaSmem *>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_launch_dependents();  // pass 2 may be scheduled as this grid drains
+    if (a.csr_ok && !__ldcg(a.csr_ok)) return;
+    const long long total = static_cast<long long>(a.rows) * a.n_chunks;
+    const int i0 = static_cast<int>(total * blockIdx.x / gridDim.x);
+    const int i1 = static_cast<int>(total * (blockIdx.x + 1) / gridDim.x);
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], kConsumerWarps);
+        }
+        for (int s = 0; s < kSegSlots; ++s) {
+            mbar_init(&sm.seg_full[s], kConsumerWarps);
+            mbar_init(&sm.seg_empty[s], 1);
+        }
+        sm.abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    volatile int *abort_flag = &sm.abort;
+    auto timeout = [&]() {
+        *abort_flag = 1;
+        atomicOr(a.status, SV_FLAG_TIMEOUT);
+    };
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            int k = 0;
+            for (int item = i0; item < i1; ++item, ++k) {
+                const int s = k % kStages;
+                if (k >= kStages && !mbar_wait_bounded(&sm.empty[s], ((k / kStages) - 1) & 1, kWaitBudget))
+                    timeout();
+                if (*abort_flag) {
+                    // let the copies already issued into the ring land before leaving
+                    for (int kk = max(0, k - kStages); kk < k; ++kk)
+                        mbar_wait_bounded(&sm.full[kk % kStages], (kk / kStages) & 1, kWaitBudget);
+                    break;
+                }
+                const int row = item / a.n_chunks;
+                const int chunk = item - row * a.n_chunks;
+                const int c0 = chunk * CHUNK;
+                const int n = min(CHUNK, a.V - c0);
+                const T *src = reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(row) * a.V + c0;
+                const uint32_t bytes = static_cast<uint32_t>(n) * sizeof(T);
+                mbar_arrive_expect_tx(&sm.full[s], bytes);
+                bulk_g2s(sm.ring[s], src, bytes, &sm.full[s]);
+            }
+        }
+        return;
+    }
+
+    if (warp == kPublisherWarp) {
+        const int n_seg = (i1 - 1) / a.n_chunks - i0 / a.n_chunks + 1;
+        for (int g = 0; g < n_seg; ++g) {
+            const int slot = g % kSegSlots;
+            if (!mbar_wait_bounded(&sm.seg_full[slot], (g / kSegSlots) & 1, kWaitBudget)) timeout();
+            if (*abort_flag) break;
+            const SegMsg msg = sm.seg[slot];
+            float ra = -INFINITY;
+            int rb = kSample ? __float_as_int(0.f) : 0x7fffffff;
+            if (lane == 0)
+                for (int w = 0; w < kConsumerWarps; ++w) merge_pair<kSample>(ra, rb, sm.segpart[slot][w]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.seg_empty[slot]);
+            // the segment's chunk partials: the merged value in its first chunk,
+            // the identity in the others
+            float2 *P = a.partials + static_cast<size_t>(msg.row) * a.n_chunks + msg.first_chunk;
+            for (int c = lane; c < msg.n_chunk; c += 32) {
+                float ia;
+                int ib;
+                partial_identity<kSample>(ia, ib);
+                P[c] = (c == 0) ? make_float2(ra, __int_as_float(rb)) : make_float2(ia, __int_as_float(ib));
+            }
+            __threadfence();
+            __syncwarp();
+            int islast = 0, b = 0;
+            if (lane == 0) {
+                b = request_of_row(a, msg.row);
+                int r0, nr;
+                request_rows(a, b, r0, nr);
+                const uint32_t old = atom_add_release_gpu(a.tickets1 + b, static_cast<uint32_t>(msg.n_chunk));
+                islast = (old + msg.n_chunk == static_cast<uint32_t>(nr) * static_cast<uint32_t>(a.n_chunks));
+                if (islast) fence_acq_rel_gpu();
+            }
+            islast = __shfl_sync(0xffffffffu, islast, 0);
+            b = __shfl_sync(0xffffffffu, b, 0);
+            if (islast) decide_warp<T, kSample>(a, b, lane);
+        }
+        return;
+    }
+
+    // consumers
+    int k = 0, g = 0;
+    int seg_row = i0 / a.n_chunks;
+    int seg_first = i0 - seg_row * a.n_chunks;
+    int seg_n = 0;
+    float ra;
+    int rb;
+    partial_identity<kSample>(ra, rb);
+    auto post = [&]() -> bool {
+        float wa = ra;
+        int wb = rb;
+        warp_partial_reduce<kSample>(wa, wb);
+        const int slot = g % kSegSlots;
+        if (g >= kSegSlots && !mbar_wait_bounded(&sm.seg_empty[slot], ((g / kSegSlots) - 1) & 1, kWaitBudget))
+            timeout();
+        if (*abort_flag) return false;
+        if (lane == 0) {
+            sm.segpart[slot][warp] = make_float2(wa, __int_as_float(wb));
+            if (warp == 0) sm.seg[slot] = SegMsg{seg_row, seg_first, seg_n, 0};
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.seg_full[slot]);
+        ++g;
+        return true;
+    };
+    for (int item = i0; item < i1; ++item, ++k) {
+        const int row = item / a.n_chunks;
+        const int chunk = item - row * a.n_chunks;
+        if (row != seg_row) {
+            if (!post()) return;
+            seg_row = row;
+            seg_first = chunk;
+            seg_n = 0;
+            partial_identity<kSample>(ra, rb);
+        }
+        const int s = k % kStages;
+        if (!mbar_wait_bounded(&sm.full[s], (k / kStages) & 1, kWaitBudget)) timeout();
+        if (*abort_flag) return;
+        const int c0 = chunk * CHUNK;
+        const int n = min(CHUNK, a.V - c0);
+        const uint4 *stage = reinterpret_cast<const uint4 *>(sm.ring[s]);
+        float vals[kTmaVecs][VEC];
+        int e0[kTmaVecs];
+#pragma unroll
+        for (int j = 0; j < kTmaVecs; ++j) {
+            const int v = warp * (kTmaVecs * 32) + j * 32 + lane;
+            e0[j] = v * VEC;
+            uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+            if (e0[j] < n) raw = stage[v];
+            unpack(raw, vals[j]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[s]);  // slice consumed: the stage may be refilled
+        lane_accumulate<kSample, kTmaVecs, VEC>(vals, e0, n, c0, a.c, ra, rb);
+        ++seg_n;
+    }
+    post();
+}
+
+// ---------------------------------------------------------------------------
+// Pass 1, any alignment: one CTA per (row, chunk), element loads.
+// ---------------------------------------------------------------------------
+template <typename T, bool kSample>
+__global__ void __launch_bounds__(kThreads) stats_scalar_kernel(Args a) {
+    constexpr int VEC = Elem<T>::kVec;
+    constexpr int CHUNK = chunk_elems<T>();
+    __shared__ float2 wp[kWarps];
+    pdl_launch_dependents();
+    if (a.csr_ok && !__ldcg(a.csr_ok)) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row = blockIdx.x / a.n_chunks;
+    const int chunk = blockIdx.x - row * a.n_chunks;
+    const int c0 = chunk * CHUNK;
+    const int n = min(CHUNK, a.V - c0);
+    const T *zrow = reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(row) * a.V + c0;
+    float vals[kLoadsPerThread][VEC];
+    int e0[kLoadsPerThread];
+#pragma unroll
+    for (int j = 0; j < kLoadsPerThread; ++j) {
+        e0[j] = (warp * (kLoadsPerThread * 32) + j * 32 + lane) * VEC;
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) vals[j][k] = (e0[j] + k < n) ? Elem<T>::at(zrow, e0[j] + k) : 0.f;
+    }
+    float ra;
+    int rb;
+    lane_partial<kSample, VEC>(vals, e0, n, c0, a.c, ra, rb);
+    warp_partial_reduce<kSample>(ra, rb);
+    if (lane == 0) wp[warp] = make_float2(ra, __int_as_float(rb));
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0) {
+            float ma = -INFINITY;
+            int mb = kSample ? __float_as_int(0.f) : 0x7fffffff;
+            for (int w = 0; w < kWarps; ++w) merge_pair<kSample>(ma, mb, wp[w]);
+            ra = ma;
+            rb = mb;
+        }
+        publish_partial<T, kSample>(a, row, chunk, ra, rb, lane);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Pass 2: residual masses per 1024-token tile and the inverse-CDF draw.
+// One thread-block cluster of kResCluster CTAs per request splits the
+// selected row's tiles; tile masses stay in each CTA's shared memory.  After a
+// cluster barrier, warp 0 of rank 0 reads all masses through distributed
+// shared memory, takes the prefix over tiles in fp64 and resolves the token.
+//
+// A tile is owned by one warp: lane l holds tokens tile*1024 + (j*32 + l)*4 + k,
+// j < 8, k < 4.  The running sum in token order is
+//   E(j, l, k) = (base_j + excl_j(l)) + pre_k(l),   base_{j+1} = base_j + seg_j
+// (Hillis-Steele lane scan per 128-token segment), and the tile's mass is
+// E at its last position.  The tile masses that feed the prefix are plain
+// sums of the same r values (tree + butterfly); where rounding leaves the
+// tile's running sums short of u R, the draw moves on to the next token with
+// r > 0, which is what the exact inverse CDF gives up to that rounding.
+// ---------------------------------------------------------------------------
+constexpr int kResCluster = 2;
+constexpr int kResWarps = 16;
+constexpr int kResThreads = kResWarps * 32;
+
+template <typename T> struct TileRaw;
+template <> struct TileRaw<float> {
+    float4 z[8];
+    float4 q[8];
+};
+template <> struct TileRaw<__nv_bfloat16> {
+    uint2 z[8];
+    float4 q[8];
+};
+
+// Loads of one tile (issued together so they overlap).
+template <typename T, bool kVecPath>
+__device__ __forceinline__ void warp_tile_load(const T *zrow, const float *qrow, int V, int tile, int lane,
+                                               TileRaw<T> &raw) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int e0 = tile * kTileElems + (j * 32 + lane) * 4;
+        if (kVecPath && e0 + 4 <= V) {
+            if constexpr (sizeof(T) == 4) raw.z[j] = __ldg(reinterpret_cast<const float4 *>(zrow + e0));
+            else raw.z[j] = __ldg(reinterpret_cast<const uint2 *>(zrow + e0));
+            raw.q[j] = qrow ? __ldg(reinterpret_cast<const float4 *>(qrow + e0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            float zz[4], qq[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int e = e0 + k;
+                zz[k] = (e < V) ? Elem<T>::at(zrow, e) : -INFINITY;
+                qq[k] = (qrow && e < V) ? __ldg(qrow + e) : 0.f;
+            }
+            if constexpr (sizeof(T) == 4) {
+                raw.z[j] = make_float4(zz[0], zz[1], zz[2], zz[3]);
+            } else {
+                // bf16 values are exact in fp32: keep their upper halves
+                raw.z[j] = make_uint2((__float_as_uint(zz[0]) >> 16) | (__float_as_uint(zz[1]) & 0xffff0000u),
+                                      (__float_as_uint(zz[2]) >> 16) | (__float_as_uint(zz[3]) & 0xffff0000u));
+            }
+            raw.q[j] = make_float4(qq[0], qq[1], qq[2], qq[3]);
+        }
+    }
+}
+
+// r(v) of the tile's tokens from its loaded data.  Same arithmetic (no
+// contraction) wherever it is called.
+template <typename T>
+__device__ __forceinline__ void warp_tile_compute(const TileRaw<T> &raw, bool has_q, int V, int tile, float c,
+                                                  float M, float invS, int lane, float (&r)[8][4]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int e0 = tile * kTileElems + (j * 32 + lane) * 4;
+        float z[4];
+        if constexpr (sizeof(T) == 4) {
+            z[0] = raw.z[j].x; z[1] = raw.z[j].y; z[2] = raw.z[j].z; z[3] = raw.z[j].w;
+        } else {
+            z[0] = __uint_as_float(raw.z[j].x << 16);
+            z[1] = __uint_as_float(raw.z[j].x & 0xffff0000u);
+            z[2] = __uint_as_float(raw.z[j].y << 16);
+            z[3] = __uint_as_float(raw.z[j].y & 0xffff0000u);
+        }
+        const float qv[4] = {raw.q[j].x, raw.q[j].y, raw.q[j].z, raw.q[j].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int e = e0 + k;
-            z[k] = (e < V) ? Elem<T>::at(zrow, e) : -INFINITY;
-            if (qrow) qv[k] = (e < V) ? __ldg(qrow + e) : 0.f;
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        if (e0 + k < V) {
-            const float p = __fmul_rn(ex2(__fmaf_rn(z[k], c, -M)), invS);
-            r[k] = qrow ? fmaxf(__fsub_rn(p, qv[k]), 0.f) : p;
-        } else {
-            r[k] = 0.f;
+            if (e0 + k < V) {
+                const float p = __fmul_rn(ex2(__fmaf_rn(z[k], c, -M)), invS);
+                r[j][k] = has_q ? fmaxf(__fsub_rn(p, qv[k]), 0.f) : p;
+            } else {
+                r[j][k] = 0.f;
+            }
         }
     }
 }
 
-// Running sums of the tile: e[k] = excl(thread) + (r0 + .. + rk), and the tile
-// total (the value e[3] of the last thread).  Deterministic.
-__device__ __forceinline__ float tile_scan(const float (&r)[4], float (&e)[4], ScanSmem &sm) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    float pre[4];
-    pre[0] = r[0];
-    pre[1] = __fadd_rn(pre[0], r[1]);
-    pre[2] = __fadd_rn(pre[1], r[2]);
-    pre[3] = __fadd_rn(pre[2], r[3]);
-    const float s = pre[3];
-    float incl = s;
+struct TileScan {
+    int v;       // found token (kFind) or -1
+    float rv;    // its r(v)
+    float mass;  // tile mass
+};
+
+// kFind = false: tile mass (valid in every lane).
+// kFind = true : the smallest token v < V of the tile with base + E(v) > t
+//                (or -1) and its r(v).
+template <bool kFind>
+__device__ __forceinline__ TileScan warp_tile_scan(const float (&r)[8][4], int tile, int V, double base_p,
+                                                   double t, int lane) {
+    float base = 0.f;
+    float last = 0.f;
+    TileScan res{-1, 0.f, 0.f};
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl = __fadd_rn(incl, y);
+    for (int j = 0; j < 8; ++j) {
+        float pre[4];
+        pre[0] = r[j][0];
+        pre[1] = __fadd_rn(pre[0], r[j][1]);
+        pre[2] = __fadd_rn(pre[1], r[j][2]);
+        pre[3] = __fadd_rn(pre[2], r[j][3]);
+        float incl = pre[3];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl = __fadd_rn(incl, y);
+        }
+        float lex = __shfl_up_sync(0xffffffffu, incl, 1);
+        if (lane == 0) lex = 0.f;
+        const float seg = __shfl_sync(0xffffffffu, incl, 31);
+        const float head = __fadd_rn(base, lex);
+        if (kFind) {
+            int cand = -1;
+            const int e0 = tile * kTileElems + (j * 32 + lane) * 4;
+#pragma unroll
+            for (int k = 3; k >= 0; --k)
+                if (e0 + k < V && base_p + static_cast<double>(__fadd_rn(head, pre[k])) > t) cand = k;
+            const unsigned m = __ballot_sync(0xffffffffu, cand >= 0);
+            if (m && res.v < 0) {  // first segment holding a crossing (no early exit: keeps r in registers)
+                const int src = __ffs(m) - 1;
+                const int ck = __shfl_sync(0xffffffffu, cand, src);
+                float rsel = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (k == ck) rsel = r[j][k];
+                res.v = tile * kTileElems + (j * 32 + src) * 4 + ck;
+                res.rv = __shfl_sync(0xffffffffu, rsel, src);
+            }
+        }
+        if (j == 7) last = __shfl_sync(0xffffffffu, __fadd_rn(head, pre[3]), 31);
+        base = __fadd_rn(base, seg);
     }
-    float lane_excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) lane_excl = 0.f;
-    __syncthreads();  // protect warp_tot / tile_total from a previous use
-    if (lane == 31) sm.warp_tot[warp] = incl;
-    __syncthreads();
-    float woff = 0.f;
-    for (int w = 0; w < warp; ++w) woff = __fadd_rn(woff, sm.warp_tot[w]);
-    const float excl = __fadd_rn(woff, lane_excl);
+    res.mass = last;
+    return res;
+}
+
+// Tile mass for the prefix: per-lane tree over its 32 values, butterfly
+// across lanes (the running sums of the draw are taken separately, in token
+// order, on the one tile the draw lands in).
+__device__ __forceinline__ float warp_tile_sum(const float (&r)[8][4]) {
+    float v[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) e[k] = __fadd_rn(excl, pre[k]);
-    if (tid == kThreads - 1) sm.tile_total = e[3];
-    __syncthreads();
-    return sm.tile_total;
+    for (int j = 0; j < 8; ++j) v[j] = (r[j][0] + r[j][1]) + (r[j][2] + r[j][3]);
+#pragma unroll
+    for (int w = 1; w < 8; w <<= 1)
+#pragma unroll
+        for (int j = 0; j + w < 8; j += 2 * w) v[j] += v[j + w];
+    float x = v[0];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
 }
 
 template <typename T, bool kVecPath>
-__device__ void draw_final(const Args &a, int b, const Decision &d, ScanSmem &sm) {
-    const int tid = threadIdx.x, lane = tid & 31;
+__device__ __forceinline__ float tile_mass_of(const T *zrow, const float *qrow, int V, int tile, const Decision &d,
+                                              float c, int lane, float (&r)[8][4]) {
+    TileRaw<T> raw;
+    warp_tile_load<T, kVecPath>(zrow, qrow, V, tile, lane, raw);
+    warp_tile_compute<T>(raw, qrow != nullptr, V, tile, c, d.M, d.invS, lane, r);
+    return warp_tile_sum(r);
+}
+
+// The draw (warp 0 of the cluster's rank 0).  Tile i's mass lives in the
+// shared memory of rank i / per at index i % per; the slow paths keep theirs
+// in the workspace.
+template <typename T, bool kVecPath>
+__device__ __forceinline__ void draw_final(const Args &a, int b, const Decision d, int lane, const float *smass,
+                                           int per) {
     const T *zrow = reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(d.row) * a.V;
     const float *qrow = (d.qrow >= 0) ? a.q + static_cast<size_t>(d.qrow) * a.V : nullptr;
-    const float *mass = a.tile_mass + static_cast<size_t>(b) * a.n_tiles;
-    if (tid == 0) sm.zero_fallback = 0;
-
+    float *gmass = a.tile_mass + static_cast<size_t>(b) * a.n_tiles;
+    bool from_smem = true;
+    auto mass_at = [&](int i) -> float {
+        if (!from_smem) return __ldcg(gmass + i);
+        const int owner = i / per;
+        return owner == 0 ? smass[i] : ld_dsmem_f32(smass + (i - owner * per), static_cast<uint32_t>(owner));
+    };
+    double R = 0.0, t = 0.0, fbase = 0.0;
+    int ftile = -1;
     for (int attempt = 0; attempt < 2; ++attempt) {
-        // prefix over tile masses in fp64 (warp 0); lane l owns a contiguous group
-        if (tid < 32) {
-            const int G = (a.n_tiles + 31) / 32;
-            const int i0 = min(lane * G, a.n_tiles), i1 = min(i0 + G, a.n_tiles);
-            double sum = 0.0;
-            for (int i = i0; i < i1; ++i) sum += static_cast<double>(__ldcg(mass + i));
-            double incl = sum;
+        // fp64 prefix over the tile masses; lane l owns a contiguous group
+        const int G = (a.n_tiles + 31) / 32;
+        const int i0 = min(lane * G, a.n_tiles), i1 = min(i0 + G, a.n_tiles);
+        double sum = 0.0;
+        for (int i = i0; i < i1; ++i) sum += static_cast<double>(mass_at(i));
+        double incl = sum;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const double y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const double R = __shfl_sync(0xffffffffu, incl, 31);
-            double base = __shfl_up_sync(0xffffffffu, incl, 1);  // exclusive offset of the group
-            if (lane == 0) base = 0.0;
-            const double t = static_cast<double>(d.u) * R;
-            int found = -1;
-            double fbase = 0.0, P = base;
-            for (int i = i0; i < i1; ++i) {
-                const double Pn = P + static_cast<double>(__ldcg(mass + i));
-                if (found < 0 && Pn > t) {
-                    found = i;
-                    fbase = P;
-                }
-                P = Pn;
-            }
-            const unsigned ball = __ballot_sync(0xffffffffu, found >= 0);
-            const int src = ball ? (__ffs(ball) - 1) : 0;
-            const int ft = __shfl_sync(0xffffffffu, found, src);
-            const double fb = __shfl_sync(0xffffffffu, fbase, src);
-            if (lane == 0) {
-                sm.found_tile = ball ? ft : -1;
-                sm.found_base = fb;
-                sm.R = R;
-                sm.t = t;
-            }
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
         }
-        __syncthreads();
-        if (sm.R > 0.0 || attempt == 1) break;
-        // empty residual after a rejection: draw from p instead (recompute masses)
+        R = __shfl_sync(0xffffffffu, incl, 31);
+        double P = __shfl_up_sync(0xffffffffu, incl, 1);
+        if (lane == 0) P = 0.0;
+        t = static_cast<double>(d.u) * R;
+        int found = -1;
+        double fb = 0.0;
+        for (int i = i0; i < i1; ++i) {
+            const double Pn = P + static_cast<double>(mass_at(i));
+            if (found < 0 && Pn > t) {
+                found = i;
+                fb = P;
+            }
+            P = Pn;
+        }
+        const unsigned ball = __ballot_sync(0xffffffffu, found >= 0);
+        const int src = ball ? (__ffs(ball) - 1) : 0;
+        ftile = ball ? __shfl_sync(0xffffffffu, found, src) : -1;
+        fbase = __shfl_sync(0xffffffffu, fb, src);
+        if (R > 0.0 || attempt == 1) break;
+        // empty residual after a rejection: draw from p instead (slow path)
         qrow = nullptr;
-        if (tid == 0) {
-            sm.zero_fallback = 1;
-            atomicOr(a.status, SV_FLAG_ZERO_RESIDUAL);
-        }
-        float *wmass = a.tile_mass + static_cast<size_t>(b) * a.n_tiles;
+        from_smem = false;
+        if (lane == 0) atomicOr(a.status, SV_FLAG_ZERO_RESIDUAL);
         for (int tile = 0; tile < a.n_tiles; ++tile) {
-            float r[4], e[4];
-            tile_values<T, kVecPath>(zrow, qrow, a.V, tile, a.c, d.M, d.invS, r);
-            const float tot = tile_scan(r, e, sm);
-            if (tid == 0) wmass[tile] = tot;
+            float r[8][4];
+            const float m = tile_mass_of<T, kVecPath>(zrow, qrow, a.V, tile, d, a.c, lane, r);
+            if (lane == 0) gmass[tile] = m;
         }
         __threadfence_block();
-        __syncthreads();
+        __syncwarp();
     }
-
-    if (tid == 0) {
-        sm.vbest = 0x7fffffff;
-        sm.rbest = 0.f;
-    }
-    __syncthreads();
-    const int ft = sm.found_tile;
-    if (ft >= 0) {
-        float r[4], e[4];
-        tile_values<T, kVecPath>(zrow, qrow, a.V, ft, a.c, d.M, d.invS, r);
-        tile_scan(r, e, sm);
-        const int e0 = ft * kTileElems + tid * 4;
-        int cand = 0x7fffffff;
+    int vstar = -1;
+    float rstar = 0.f;
+    if (ftile >= 0) {
+        TileRaw<T> raw;
+        float r[8][4];
+        warp_tile_load<T, kVecPath>(zrow, qrow, a.V, ftile, lane, raw);
+        warp_tile_compute<T>(raw, qrow != nullptr, a.V, ftile, a.c, d.M, d.invS, lane, r);
+        const TileScan ts = warp_tile_scan<true>(r, ftile, a.V, fbase, t, lane);
+        vstar = ts.v;
+        rstar = ts.rv;
+        // the tile's running sums ended just short of u R (rounding between the
+        // tile sum and the running sums): the next token with r > 0
+        for (int tile = ftile + 1; tile < a.n_tiles && vstar < 0; ++tile) {
+            if (!(mass_at(tile) > 0.f)) continue;
+            TileRaw<T> raw2;
+            float r2[8][4];
+            warp_tile_load<T, kVecPath>(zrow, qrow, a.V, tile, lane, raw2);
+            warp_tile_compute<T>(raw2, qrow != nullptr, a.V, tile, a.c, d.M, d.invS, lane, r2);
+            int loc = 0x7fffffff;
+            float rloc = 0.f;
 #pragma unroll
-        for (int k = 3; k >= 0; --k)
-            if (e0 + k < a.V && sm.found_base + static_cast<double>(e[k]) > sm.t) cand = e0 + k;
-        if (cand != 0x7fffffff) atomicMin(&sm.vbest, cand);
-        __syncthreads();
-        if (sm.vbest != 0x7fffffff && sm.vbest >= e0 && sm.vbest < e0 + 4) sm.rbest = r[sm.vbest - e0];
-    }
-    __syncthreads();
-    if (sm.vbest == 0x7fffffff) {
-        // rounding left u R above every boundary: the largest token with r > 0
-        int last_tile = -1;
-        for (int i = a.n_tiles - 1; i >= 0; --i)
-            if (__ldcg(mass + i) > 0.f) {
-                last_tile = i;
-                break;
-            }
-        if (last_tile >= 0) {
-            float r[4];
-            tile_values<T, kVecPath>(zrow, qrow, a.V, last_tile, a.c, d.M, d.invS, r);
-            const int e0 = last_tile * kTileElems + tid * 4;
-            int cand = -1;
+            for (int j = 7; j >= 0; --j)
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (e0 + k < a.V && r[k] > 0.f) cand = e0 + k;
-            __shared__ int s_max;
-            if (tid == 0) s_max = -1;
-            __syncthreads();
-            if (cand >= 0) atomicMax(&s_max, cand);
-            __syncthreads();
-            if (s_max >= e0 && s_max < e0 + 4) {
-                sm.vbest = s_max;
-                sm.rbest = r[s_max - e0];
+                for (int k = 3; k >= 0; --k) {
+                    const int e = (j * 32 + lane) * 4 + k;
+                    if (tile * kTileElems + e < a.V && r2[j][k] > 0.f) {
+                        loc = e;
+                        rloc = r2[j][k];
+                    }
+                }
+            const int best = __reduce_min_sync(0xffffffffu, loc);
+            if (best != 0x7fffffff) {
+                const unsigned m = __ballot_sync(0xffffffffu, loc == best);
+                rstar = __shfl_sync(0xffffffffu, rloc, __ffs(m) - 1);
+                vstar = tile * kTileElems + best;
             }
         }
-        __syncthreads();
     }
-    if (tid == 0) {
-        const int v = (sm.vbest == 0x7fffffff) ? -1 : sm.vbest;
-        a.out_tokens[d.slot] = v;
+    if (vstar < 0) {
+        // rounding left u R above every boundary: the largest token with r > 0
+        for (int tile = a.n_tiles - 1; tile >= 0 && vstar < 0; --tile) {
+            if (!(mass_at(tile) > 0.f)) continue;
+            TileRaw<T> raw;
+            float r[8][4];
+            warp_tile_load<T, kVecPath>(zrow, qrow, a.V, tile, lane, raw);
+            warp_tile_compute<T>(raw, qrow != nullptr, a.V, tile, a.c, d.M, d.invS, lane, r);
+            int loc = -1;
+            float rloc = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int e = (j * 32 + lane) * 4 + k;
+                    if (tile * kTileElems + e < a.V && r[j][k] > 0.f) {
+                        loc = e;
+                        rloc = r[j][k];
+                    }
+                }
+            const int best = __reduce_max_sync(0xffffffffu, loc);
+            if (best >= 0) {
+                const unsigned m = __ballot_sync(0xffffffffu, loc == best);
+                rstar = __shfl_sync(0xffffffffu, rloc, __ffs(m) - 1);
+                vstar = tile * kTileElems + best;
+            }
+        }
+    }
+    if (lane == 0) {
+        a.out_tokens[d.slot] = vstar;
         if (a.diag) {
-            a.diag[a.n_draft + 2 * b] = static_cast<float>(sm.R);
-            a.diag[a.n_draft + 2 * b + 1] = static_cast<float>(static_cast<double>(sm.rbest) / sm.R);
+            a.diag[a.n_draft + 2 * b] = static_cast<float>(R);
+            a.diag[a.n_draft + 2 * b + 1] = static_cast<float>(static_cast<double>(rstar) / R);
         }
     }
 }
 
 template <typename T, bool kVecPath>
-__global__ void __launch_bounds__(kThreads) residual_kernel(Args a) {
-    __shared__ ScanSmem sm;
-    __shared__ int s_last;
+__global__ void __cluster_dims__(kResCluster, 1, 1) __launch_bounds__(kResThreads, 1) residual_kernel(Args a) {
+    extern __shared__ float smass[];  // ceil(n_tiles / kResCluster) tile masses of this CTA
+    pdl_wait_prior_grid();  // decisions come from pass 1
     if (a.csr_ok && !__ldcg(a.csr_ok)) return;
-    const int b = blockIdx.x / a.n_parts;
-    const int part = blockIdx.x - b * a.n_parts;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int b = blockIdx.x / kResCluster;
     const Decision d = a.dec[b];
-    if (!d.valid) return;
+    if (!d.valid) return;  // same decision for every CTA of the cluster
     const T *zrow = reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(d.row) * a.V;
     const float *qrow = (d.qrow >= 0) ? a.q + static_cast<size_t>(d.qrow) * a.V : nullptr;
-    const int t0 = part * kTilesPerPart;
-    const int t1 = min(t0 + kTilesPerPart, a.n_tiles);
-    for (int tile = t0; tile < t1; ++tile) {
-        float r[4], e[4];
-        tile_values<T, kVecPath>(zrow, qrow, a.V, tile, a.c, d.M, d.invS, r);
-        const float tot = tile_scan(r, e, sm);
-        if (threadIdx.x == 0) a.tile_mass[static_cast<size_t>(b) * a.n_tiles + tile] = tot;
+    const int per = (a.n_tiles + kResCluster - 1) / kResCluster;
+    const int t0 = static_cast<int>(rank) * per;
+    const int t1 = min(t0 + per, a.n_tiles);
+    for (int t = t0 + warp; t < t1; t += kResWarps) {
+        float r[8][4];
+        const float m = tile_mass_of<T, kVecPath>(zrow, qrow, a.V, t, d, a.c, lane, r);
+        if (lane == 0) smass[t - t0] = m;
     }
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const uint32_t cnt = ticket_arrive(a.tickets2 + b, a.epoch);
-        s_last = (cnt == static_cast<uint32_t>(a.n_parts)) ? 1 : 0;
-        if (s_last) a.tickets2[b] = 0ull;
-    }
-    __syncthreads();
-    if (s_last) {
-        __threadfence();
-        draw_final<T, kVecPath>(a, b, d, sm);
-    }
+    cluster_sync();
+    if (rank == 0 && warp == 0) draw_final<T, kVecPath>(a, b, d, lane, smass, per);
+    cluster_sync();  // every CTA's shared memory stays alive until rank 0 has read it
 }
 
 // ---------------------------------------------------------------------------
@@ -590,10 +973,17 @@ __global__ void __launch_bounds__(kThreads) csr_check_kernel(Args a, int *csr_ok
 // Host side
 // ---------------------------------------------------------------------------
 struct WsLayout {
-    size_t status, csr_ok, tickets1, tickets2, dec, partials, tile_mass, total;
+    size_t status, csr_ok, tickets1, dec, partials, tile_mass, total;
 };
 
 static inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Per-request counters live in a region of fixed capacity right after the
+// status words, whatever the call's shape, and every completed call leaves
+// the counters it used at zero.  A workspace therefore serves calls of any
+// shape once it has been zero-filled; only a call with more than kTicketCap
+// requests (whose counters reach into other regions) clears them first.
+constexpr int kTicketCap = 16384;
 
 static WsLayout ws_layout(int B, int rows, int V) {
     WsLayout L;
@@ -602,8 +992,7 @@ static WsLayout ws_layout(int B, int rows, int V) {
     size_t o = 0;
     L.status = o; o = align256(o + 16);
     L.csr_ok = o; o = align256(o + 16);
-    L.tickets1 = o; o = align256(o + 8ull * B);
-    L.tickets2 = o; o = align256(o + 8ull * B);
+    L.tickets1 = o; o = align256(o + 4ull * static_cast<size_t>(B > kTicketCap ? B : kTicketCap));
     L.dec = o; o = align256(o + sizeof(Decision) * static_cast<size_t>(B));
     L.partials = o; o = align256(o + sizeof(float2) * static_cast<size_t>(rows) * n_chunks);
     L.tile_mass = o; o = align256(o + sizeof(float) * static_cast<size_t>(B) * n_tiles);
@@ -611,25 +1000,10 @@ static WsLayout ws_layout(int B, int rows, int V) {
     return L;
 }
 
-// Call epochs start from a per-process value so that two copies of the
-// library, or a workspace holding leftovers, do not share a tag sequence.
-static uint32_t initial_epoch() {
-    static int anchor;
-    uint32_t x = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&anchor) & 0xffffffffu);
-    x ^= static_cast<uint32_t>(std::chrono::steady_clock::now().time_since_epoch().count());
-    x ^= static_cast<uint32_t>(getpid()) * 2654435761u;
-    return x ? x : 1u;
-}
-static std::atomic<uint32_t> g_epoch{initial_epoch()};
 static void *g_prof_begin = nullptr;
 static void *g_prof_end = nullptr;
 static thread_local int g_last_launches = 0;
 
-uint32_t next_epoch() {
-    uint32_t e = g_epoch.fetch_add(1, std::memory_order_relaxed);
-    if (e == 0) e = g_epoch.fetch_add(1, std::memory_order_relaxed);
-    return e;
-}
 void prof_begin(cudaStream_t s) {
     if (g_prof_begin) cudaEventRecord(static_cast<cudaEvent_t>(g_prof_begin), s);
 }
@@ -638,31 +1012,76 @@ void prof_end(cudaStream_t s) {
 }
 void set_launches(int n) { g_last_launches = n; }
 
-template <typename T, bool kSample, bool kVecPath>
-static void launch_pass1(const Args &a, cudaStream_t s) {
-    const unsigned grid = static_cast<unsigned>(a.rows) * static_cast<unsigned>(a.n_chunks);
-    stats_decide_kernel<T, kSample, kVecPath><<<grid, kThreads, 0, s>>>(a);
+// Number of SMs of the current device (queried once per device).
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!cached[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 1;
+    }
+    return cached[dev];
 }
 
+template <typename T, bool kSample>
+static void launch_tma_pass1(const Args &a, cudaStream_t s) {
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!configured[dev]) {
+        cudaFuncSetAttribute(stats_tma_kernel<T, kSample>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(TmaSmem)));
+        configured[dev] = true;
+    }
+    const long long items = static_cast<long long>(a.rows) * a.n_chunks;
+    const unsigned grid = static_cast<unsigned>(items < sm_count() ? items : sm_count());
+    stats_tma_kernel<T, kSample><<<grid, kTmaThreads, sizeof(TmaSmem), s>>>(a);
+}
+
+template <typename T, bool kSample>
+static void launch_scalar_pass1(const Args &a, cudaStream_t s) {
+    const unsigned grid = static_cast<unsigned>(a.rows) * static_cast<unsigned>(a.n_chunks);
+    stats_scalar_kernel<T, kSample><<<grid, kThreads, 0, s>>>(a);
+}
+
+// Pass 2 is launched as a programmatic dependent of pass 1: its CTAs may be
+// scheduled while pass 1 drains and wait (griddepcontrol.wait) for pass 1's
+// completion before reading the decisions.
 template <typename T, bool kVecPath>
 static void launch_pass2(const Args &a, cudaStream_t s) {
-    const unsigned grid = static_cast<unsigned>(a.B) * static_cast<unsigned>(a.n_parts);
-    residual_kernel<T, kVecPath><<<grid, kThreads, 0, s>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.B) * kResCluster);
+    cfg.blockDim = dim3(kResThreads);
+    cfg.dynamicSmemBytes = sizeof(float) * static_cast<size_t>((a.n_tiles + kResCluster - 1) / kResCluster);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, residual_kernel<T, kVecPath>, a);
 }
 
 template <typename T>
 static sv_status run_typed(Args &a, bool sample, bool vec, cudaStream_t s) {
     a.n_chunks = (a.V + chunk_elems<T>() - 1) / chunk_elems<T>();
     int launches = 0;
+    if (a.B > kTicketCap &&
+        cudaMemsetAsync(a.tickets1, 0, sizeof(uint32_t) * static_cast<size_t>(a.B), s) != cudaSuccess)
+        return SV_ERR_CUDA;
     if (a.row_offsets) {
         csr_check_kernel<<<1, kThreads, 0, s>>>(a, const_cast<int *>(a.csr_ok));
         ++launches;
     }
     prof_begin(s);
     if (sample) {
-        if (vec) launch_pass1<T, true, true>(a, s); else launch_pass1<T, true, false>(a, s);
+        if (vec) launch_tma_pass1<T, true>(a, s); else launch_scalar_pass1<T, true>(a, s);
     } else {
-        if (vec) launch_pass1<T, false, true>(a, s); else launch_pass1<T, false, false>(a, s);
+        if (vec) launch_tma_pass1<T, false>(a, s); else launch_scalar_pass1<T, false>(a, s);
     }
     prof_end(s);
     ++launches;
@@ -711,14 +1130,11 @@ static sv_status verify_common(const void *logits, sv_dtype dt, const float *q,
     a.V = V;
     a.rows = rows;
     a.n_tiles = (V + kTileElems - 1) / kTileElems;
-    a.n_parts = (a.n_tiles + kTilesPerPart - 1) / kTilesPerPart;
     a.n_draft = rows - B;
     a.c = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(temperature)) : 1.f;
-    a.epoch = next_epoch();
     a.status = reinterpret_cast<uint32_t *>(w + L.status);
     a.csr_ok = row_offsets ? reinterpret_cast<const int *>(w + L.csr_ok) : nullptr;
-    a.tickets1 = reinterpret_cast<unsigned long long *>(w + L.tickets1);
-    a.tickets2 = reinterpret_cast<unsigned long long *>(w + L.tickets2);
+    a.tickets1 = reinterpret_cast<uint32_t *>(w + L.tickets1);
     a.dec = reinterpret_cast<Decision *>(w + L.dec);
     a.partials = reinterpret_cast<float2 *>(w + L.partials);
     a.tile_mass = reinterpret_cast<float *>(w + L.tile_mass);

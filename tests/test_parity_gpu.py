@@ -301,3 +301,25 @@ def test_emitted_token_law_chisquare_gpu(cuda_device, variant):
         pv.append(_chisq_pvalue(counts, p[j]))
     record(f"chi-square GPU {variant}", {"pvalues": pv, "trials": n, "mean_al": float(al.mean())})
     assert min(pv) > 1e-3
+
+
+def test_one_workspace_serves_calls_of_any_shape(cuda_device):
+    """A workspace zero-filled once and then used by calls of other shapes
+    (it holds their leftovers) gives the same results as a fresh one."""
+    dev = cuda_device
+    shapes = [(40, 4, 9000), (3, 2, 1000), (64, 7, 20000), (1, 0, 300), (50, 5, 12000)]
+    batches = [_rand_batch(300 + i, B=Bn, K=K, V=V, dtype=torch.float32, T=1.0)
+               for i, (Bn, K, V) in enumerate(shapes)]
+    big = max(B_.spec_verify_workspace_size(b.B, b.rows, b.V) for b in batches)
+    shared = B_.workspace(big, dev)
+    for rep in range(2):
+        for b in batches:
+            args = (b.logits.to(dev), b.q.to(dev), b.B, b.K, b.V, 1.0, b.draft.to(dev), b.uniforms.to(dev))
+            o1 = torch.empty(b.rows, dtype=torch.int32, device=dev)
+            a1 = torch.empty(b.B, dtype=torch.int32, device=dev)
+            B_.spec_verify_sample(*args, o1, a1, shared)
+            o2 = torch.empty_like(o1)
+            a2 = torch.empty_like(a1)
+            B_.spec_verify_sample(*args, o2, a2, B_.workspace(B_.spec_verify_workspace_size(b.B, b.rows, b.V), dev))
+            torch.cuda.synchronize()
+            assert torch.equal(o1, o2) and torch.equal(a1, a2), (rep, b.B, b.K, b.V)
