@@ -165,6 +165,31 @@ sv_status spec_lmhead_verify(const void *hidden, const void *w_vocab_t, int d, c
                              float *diag, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * spec_verify_sample for callers that cannot allocate device memory.  The
+ * pages have no counterpart to this call; it exists for host programs with
+ * no allocator to hand, e.g. a plugin inside an inference server whose
+ * device memory is all held by the server's caching allocator, or a loop
+ * that must not call cudaMalloc because it can synchronise the device.
+ *   Arguments and results are those of spec_verify_sample without the
+ *   workspace: the caller still passes inputs and outputs (device memory).
+ *   Scratch is a fixed array of SV_NOALLOC_SCRATCH_BYTES inside this
+ *   library, held on every GPU that loads it until the process exits.
+ *   Returns SV_ERR_WORKSPACE when the call would need more than that
+ *   (spec_verify_workspace_size(B, B (K+1), V) > SV_NOALLOC_SCRATCH_BYTES).
+ *   The first call on each device looks up the array's device address with
+ *   that device current; make that first call before any stream capture.
+ *   Every call on a device shares the one array and clears the parts that
+ *   must start at zero, so calls that overlap on the GPU race with each
+ *   other: serialise them (one stream, or events).  Device-detected input
+ *   errors show only as AL = 0 / -1 outputs; the status word cannot be read.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define SV_NOALLOC_SCRATCH_BYTES (2u << 20)
+sv_status spec_verify_sample_noalloc(const void *logits, sv_dtype dt, const float *q, int B, int K, int V,
+                                     float temperature, const int32_t *draft, const float *uniforms,
+                                     int32_t *out_tokens, int32_t *accept_len, float *diag, void *stream);
+
+/*
  * Synchronises `stream` and returns in *flags (SV_FLAG_* bits, may be NULL)
  * the device status word of workspace `ws` (the OR of every call since the
  * last read), then clears it.  Returns

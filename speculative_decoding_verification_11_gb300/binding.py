@@ -24,6 +24,7 @@ EXPORTS = (
     "spec_verify_workspace_size", "spec_verify_greedy", "spec_verify_sample", "spec_verify_ragged",
     "spec_lmhead_workspace_size", "spec_lmhead_verify", "spec_verify_last_device_status",
     "spec_status_string", "spec_profile_set_events", "spec_last_launch_count",
+    "spec_verify_sample_noalloc",
 )
 
 _lock = threading.Lock()
@@ -62,6 +63,7 @@ def load() -> ctypes.CDLL:
             "spec_status_string": (ctypes.c_char_p, [I]),
             "spec_profile_set_events": (I, [P, P]),
             "spec_last_launch_count": (I, []),
+            "spec_verify_sample_noalloc": (I, [P, I, P, I, I, I, F, P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -177,6 +179,25 @@ def spec_lmhead_verify(hidden, w_vocab_t, d, q, B, K, V, temperature, draft, uni
                                    _ptr(out_tokens), _ptr(accept_len), _ptr(diag), _ptr(ws),
                                    ws.numel(), _stream(stream))
     _raise(st, "spec_lmhead_verify")
+
+
+def spec_verify_sample_noalloc(logits, q, B, K, V, temperature, draft, uniforms, out_tokens, accept_len,
+                               diag=None, stream=None):
+    """spec_verify_sample without a workspace: for callers that cannot allocate
+    device memory; the library's own fixed scratch array is used instead."""
+    _check(q, torch.float32, B * K * V, "q")
+    _check(draft, torch.int32, B * K, "draft")
+    _check(uniforms, torch.float32, B * (K + 1), "uniforms")
+    _check(out_tokens, torch.int32, B * (K + 1), "out_tokens")
+    _check(accept_len, torch.int32, B, "accept_len")
+    st = load().spec_verify_sample_noalloc(_ptr(logits), _dtype_code(logits), _ptr(q), B, K, V,
+                                           float(temperature), _ptr(draft), _ptr(uniforms),
+                                           _ptr(out_tokens), _ptr(accept_len), _ptr(diag),
+                                           _stream(stream))
+    _raise(st, "spec_verify_sample_noalloc")
+
+
+NOALLOC_SCRATCH_BYTES = 2 << 20
 
 
 def spec_verify_last_device_status(ws, stream=None):

@@ -1000,6 +1000,14 @@ static WsLayout ws_layout(int B, int rows, int V) {
     return L;
 }
 
+// Byte range [offset, offset + bytes) of the per-request counters inside a
+// workspace laid out for (B, rows, V).
+void counter_region(int B, int rows, int V, size_t *offset, size_t *bytes) {
+    const WsLayout L = ws_layout(B, rows, V);
+    *offset = L.tickets1;
+    *bytes = L.dec - L.tickets1;
+}
+
 static void *g_prof_begin = nullptr;
 static void *g_prof_end = nullptr;
 static thread_local int g_last_launches = 0;
