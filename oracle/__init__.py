@@ -51,7 +51,8 @@ def _load():
             lib = ctypes.CDLL(build())
             P = ctypes.c_void_p
             lib.oracle_verify_batch.argtypes = [P, ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int64,
-                                                ctypes.c_double, ctypes.c_int, P, P, P, P, P, P, P]
+                                                ctypes.c_double, ctypes.c_int, P, P, P, P, P, P, P,
+                                                ctypes.c_double]
             lib.oracle_verify_batch.restype = ctypes.c_int
             lib.oracle_softmax_row.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_double, P]
             lib.oracle_softmax_row.restype = None
@@ -91,7 +92,8 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
-def verify(logits, q, draft, uniforms, row_offsets, temperature: float, greedy: bool = False):
+def verify(logits, q, draft, uniforms, row_offsets, temperature: float, greedy: bool = False,
+           tie_band: float = 1e-6):
     """Run the oracle over a CSR batch.
 
     logits  (R, V) fp32 / bf16 / fp64;  q (R - B, V) fp32 (ignored if greedy);
@@ -129,7 +131,7 @@ def verify(logits, q, draft, uniforms, row_offsets, temperature: float, greedy: 
     rc = lib.oracle_verify_batch(_ptr(z), zcode, _ptr(qa), _ptr(ro), B, V,
                                  float(temperature if not greedy else 1.0), int(bool(greedy)),
                                  _ptr(x), _ptr(ua), _ptr(out), _ptr(al), _ptr(pd), _ptr(req),
-                                 _ptr(flags))
+                                 _ptr(flags), float(tie_band))
     if rc < 0:
         raise ValueError("malformed row_offsets")
     flags = flags.reshape(B, 3)
@@ -146,9 +148,10 @@ def verify(logits, q, draft, uniforms, row_offsets, temperature: float, greedy: 
     }
 
 
-def verify_fixed(logits, q, draft, uniforms, B: int, K: int, temperature: float, greedy=False):
+def verify_fixed(logits, q, draft, uniforms, B: int, K: int, temperature: float, greedy=False,
+                 tie_band: float = 1e-6):
     ro = (np.arange(B + 1, dtype=np.int32) * (K + 1)).astype(np.int32)
-    return verify(logits, q, draft, uniforms, ro, temperature, greedy)
+    return verify(logits, q, draft, uniforms, ro, temperature, greedy, tie_band)
 
 
 def softmax_rows(z, temperature: float) -> np.ndarray:
@@ -194,8 +197,12 @@ def lmhead_logits(hidden, w_vocab_t, rows=None, v_chunk: int = 8192) -> np.ndarr
     return out
 
 
-def lmhead_verify(hidden, w_vocab_t, q, draft, uniforms, B: int, K: int, temperature: float):
-    """Fused front end + verification: fp64 GEMM, then the same steps as verify()."""
+def lmhead_verify(hidden, w_vocab_t, q, draft, uniforms, B: int, K: int, temperature: float,
+                  tie_band: float = 1e-6):
+    """Fused front end + verification: fp64 GEMM, then the same steps as verify().
+    Returns the verify() dict plus the fp64 logits under "logits"."""
     z = lmhead_logits(hidden, w_vocab_t)
     greedy = temperature == 0
-    return verify_fixed(z, q, draft, uniforms, B, K, temperature if not greedy else 1.0, greedy)
+    res = verify_fixed(z, q, draft, uniforms, B, K, temperature if not greedy else 1.0, greedy, tie_band)
+    res["logits"] = z
+    return res

@@ -33,8 +33,10 @@
  *   - a drafted id outside [0, V) invalidates its request: AL = 0, all -1.
  *
  * Near ties (decisions the parity rule lets differ) are flagged here in fp64:
- *   accept test: q > 0 and |u - p/q| < 1e-6;
- *   final sample: a CDF boundary C(v)/R within 1e-6 of u.
+ *   accept test: q > 0 and |u - p/q| < band;
+ *   final sample: a CDF boundary C(v)/R within band of u;
+ * band = 1e-6 unless the caller passes another (the fused LM-head path, whose
+ * logits carry the GEMM's fp32 accumulation error, uses a wider one).
  */
 #include <math.h>
 #include <stdint.h>
@@ -45,7 +47,7 @@
 #define OR_BF16 1
 #define OR_F64 2
 
-#define NEAR_TIE 1e-6
+#define NEAR_TIE_DEFAULT 1e-6
 
 /* Read element i of a logits buffer as fp64 (bf16 and fp32 decode exactly). */
 static double logit_at(const void *base, int dtype, int64_t i)
@@ -119,7 +121,7 @@ int64_t oracle_argmax_row(const void *z, int dtype, int64_t V)
 int oracle_verify_request(const void *z, int zdtype, const float *q, const int32_t *x,
                           const float *u, int K, int64_t V, double T, int greedy,
                           int32_t *out, int32_t *al, double *p_draft, double *req,
-                          int32_t *flags, double *work)
+                          int32_t *flags, double *work, double tie_band)
 {
     for (int j = 0; j <= K; ++j)
         out[j] = -1;
@@ -158,7 +160,7 @@ int oracle_verify_request(const void *z, int zdtype, const float *q, const int32
         double qj = (double)q[(int64_t)j * V + x[j]];
         double uj = (double)u[j];
         p_draft[j] = pj;
-        if (qj > 0.0 && fabs(uj - pj / qj) < NEAR_TIE)
+        if (qj > 0.0 && fabs(uj - pj / qj) < tie_band)
             flags[0] += 1;
         if (!(uj * qj <= pj)) {
             kstar = j;
@@ -212,7 +214,7 @@ int oracle_verify_request(const void *z, int zdtype, const float *q, const int32
             }
         }
         flags[1] = 1;
-    } else if (ufin - Cprev / R < NEAR_TIE || C / R - ufin < NEAR_TIE) {
+    } else if (ufin - Cprev / R < tie_band || C / R - ufin < tie_band) {
         flags[1] = 1;
     }
     out[kstar] = (int32_t)vstar;
@@ -233,8 +235,11 @@ int oracle_verify_request(const void *z, int zdtype, const float *q, const int32
 int oracle_verify_batch(const void *logits, int zdtype, const float *q,
                         const int32_t *row_offsets, int B, int64_t V, double T, int greedy,
                         const int32_t *draft, const float *uniforms, int32_t *out_tokens,
-                        int32_t *accept_len, double *p_draft, double *req, int32_t *flags)
+                        int32_t *accept_len, double *p_draft, double *req, int32_t *flags,
+                        double tie_band)
 {
+    if (!(tie_band > 0.0))
+        tie_band = NEAR_TIE_DEFAULT;
     if (row_offsets[0] != 0)
         return -1;
     for (int b = 0; b < B; ++b)
@@ -254,7 +259,7 @@ int oracle_verify_batch(const void *logits, int zdtype, const float *q,
         float dummy_u[1] = {0.5f};
         bad += oracle_verify_request(z, zdtype, qb, draft + d0, ub ? ub : dummy_u, K, V, T,
                                      greedy, out_tokens + r0, accept_len + b, p_draft + d0,
-                                     req + 2 * b, flags + 3 * b, work);
+                                     req + 2 * b, flags + 3 * b, work, tie_band);
     }
     free(work);
     return bad;

@@ -1,10 +1,444 @@
-// Fused LM-head front end (tcgen05/TMEM GEMM with a verifier epilogue).
+// Fused LM-head front end (sm_103a): z = hidden . W_vocab on the 5th-generation
+// tensor cores, with the verifier's per-row statistics taken in the epilogue.
+//
+// This is the GEMM whose M grows from B to B (1 + D) under speculation
+// ("Co-Designing AI Models Using Speculative Decoding", Guideline 1): all
+// M = B (K+1) <= 128 rows of hidden are one tcgen05 M tile, and the kernel
+// streams W_vocab (kept as its transpose, V x d, K-major) once.
+//
+// Persistent CTA per SM over 256-wide vocabulary tiles:
+//   warp 0    TMA producer: 128 x 64 hidden tile + 256 x 64 W tile per stage
+//             (128-byte swizzle), 4-stage ring (full/empty mbarriers); W is
+//             streamed with an evict-first L2 hint, hidden with evict-last.
+//   warp 1    TMEM allocator and single-thread MMA issuer: 4 tcgen05.mma
+//             (kind::f16, bf16 x bf16 -> fp32, M=128, N=256, K=16) per stage
+//             into one of two 256-column TMEM accumulators; tcgen05.commit
+//             frees the stage and, after the last k step, publishes the tile.
+//   warps 2-5 epilogue: tcgen05.ld of the accumulator (thread = row), per row
+//             and tile the partial (M, s) = (max z c, sum 2^(z c - M)) or
+//             (max z, first argmax), and in sampling mode an fp32 copy of the
+//             tile's logits for the decide gathers and the residual draw.
+// The decide step and the residual draw then run over these partials and
+// logits (finish_from_partials in verify.cu).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+
 #include "../../include/specverify.h"
+#include "sv_device.cuh"
+#include "sv_host.h"
 
-extern "C" size_t spec_lmhead_workspace_size(int, int, int, int) { return 256; }
+namespace sv {
+namespace lm {
 
-extern "C" sv_status spec_lmhead_verify(const void *, const void *, int, const float *, int, int,
-                                        int, float, const int32_t *, const float *, int32_t *,
-                                        int32_t *, float *, void *, size_t, void *) {
-    return SV_ERR_INVALID;
+constexpr int BM = 128;                 // rows of the M tile (all rows of the batch)
+constexpr int BN = 256;                 // vocabulary entries per tile
+constexpr int BK = 64;                  // hidden-size slice per stage: 128 bytes of bf16
+constexpr int UK = 16;                  // K of one tcgen05.mma kind::f16
+constexpr int kStagesLm = 4;
+constexpr int kABytes = BM * BK * 2;    // 16 KB
+constexpr int kBBytes = BN * BK * 2;    // 32 KB
+constexpr int kTmemCols = 2 * BN;       // two fp32 accumulators of BN columns
+constexpr int kEpiWarps = 4;
+constexpr int kThreadsLm = (2 + kEpiWarps) * 32;
+constexpr long long kLmWaitBudget = 4000000000ll;
+
+// tcgen05 instruction descriptor, kind::f16: D f32, A bf16, B bf16, both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                            (static_cast<uint32_t>(BM >> 4) << 24);
+
+struct LmSmem {
+    alignas(1024) unsigned char a[kStagesLm][kABytes];
+    alignas(1024) unsigned char b[kStagesLm][kBBytes];
+    uint64_t full[kStagesLm];
+    uint64_t empty[kStagesLm];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+struct LmArgs {
+    int M, d, V, n_tiles;
+    float c;          // log2(e) / T
+    float *spill;     // M x V fp32 logits (sampling), or nullptr
+    float2 *partials; // M x n_tiles
+    uint32_t *status;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), sm_100 form.
+__device__ __forceinline__ uint64_t smem_desc_sw128(const void *p) {
+    const uint64_t addr = smem_addr(p);
+    uint64_t d = 0;
+    d |= (addr >> 4) & 0x3FFFull;        // start address, 16-byte units
+    d |= 1ull << 16;                     // leading byte offset (unused for swizzled K-major)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;  // stride byte offset
+    d |= 1ull << 46;                     // descriptor version
+    d |= 2ull << 61;                     // 128-byte swizzle
+    return d;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every tcgen05.mma this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(bar))
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+template <bool kSample>
+__global__ void __launch_bounds__(kThreadsLm, 1)
+    lmhead_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, LmArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    LmSmem &sm = *reinterpret_cast<LmSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nk = a.d / BK;
+    if (tid == 0) {
+        for (int s = 0; s < kStagesLm; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.acc_full[i], 1);
+            mbar_init(&sm.acc_empty[i], kEpiWarps);
+        }
+        mbar_init(&sm.mma_done, 1);
+        sm.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(&sm.tmem_base, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    volatile int *abort_flag = &sm.abort;
+    auto timeout = [&]() {
+        *abort_flag = 1;
+        atomicOr(a.status, SV_FLAG_TIMEOUT);
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_h = l2_policy_evict_last();
+            int kg = 0;
+            for (int t = blockIdx.x; t < a.n_tiles && !*abort_flag; t += gridDim.x) {
+                for (int kb = 0; kb < nk; ++kb, ++kg) {
+                    const int s = kg % kStagesLm;
+                    if (kg >= kStagesLm &&
+                        !mbar_wait_bounded(&sm.empty[s], ((kg / kStagesLm) - 1) & 1, kLmWaitBudget)) {
+                        timeout();
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&sm.full[s], kABytes + kBBytes);
+                    tma_load_2d(sm.a[s], &tmA, kb * BK, 0, &sm.full[s], pol_h);
+                    tma_load_2d(sm.b[s], &tmB, kb * BK, t * BN, &sm.full[s], pol_w);
+                }
+            }
+            // let every copy issued into the ring land before the CTA can leave
+            for (int kk = max(0, kg - kStagesLm); kk < kg; ++kk)
+                mbar_wait_bounded(&sm.full[kk % kStagesLm], (kk / kStagesLm) & 1, kLmWaitBudget);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int kg = 0, ti = 0;
+            for (int t = blockIdx.x; t < a.n_tiles && !*abort_flag; t += gridDim.x, ++ti) {
+                const int buf = ti & 1;
+                if (ti >= 2 && !mbar_wait_bounded(&sm.acc_empty[buf], ((ti / 2) - 1) & 1, kLmWaitBudget)) {
+                    timeout();
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * BN);
+                bool ok = true;
+                for (int kb = 0; kb < nk; ++kb, ++kg) {
+                    const int s = kg % kStagesLm;
+                    if (!mbar_wait_bounded(&sm.full[s], (kg / kStagesLm) & 1, kLmWaitBudget)) {
+                        timeout();
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = smem_desc_sw128(sm.a[s]);
+                    const uint64_t bd = smem_desc_sw128(sm.b[s]);
+#pragma unroll
+                    for (int kk = 0; kk < BK / UK; ++kk)  // advance 32 bytes (16 bf16) inside the swizzle atom
+                        tc_mma(d_tmem, ad + 2ull * kk, bd + 2ull * kk, kIdesc, (kb | kk) ? 1u : 0u);
+                    tc_commit(&sm.empty[s]);
+                }
+                if (!ok) break;
+                tc_commit(&sm.acc_full[buf]);
+            }
+            // all issued MMAs complete before TMEM is released
+            tc_commit(&sm.mma_done);
+            mbar_wait_bounded(&sm.mma_done, 0, kLmWaitBudget);
+        }
+    } else {
+        // epilogue: warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const bool live = row < a.M;
+        const bool vec_store = (a.V & 3) == 0;
+        int ti = 0;
+        for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++ti) {
+            const int buf = ti & 1;
+            if (!mbar_wait_bounded(&sm.acc_full[buf], (ti / 2) & 1, kLmWaitBudget)) timeout();
+            if (*abort_flag) break;
+            tc_fence_after();
+            const int n0 = t * BN;
+            float Mr = -INFINITY, Sr = 0.f;
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+#pragma unroll 1
+            for (int cb = 0; cb < BN / 32; ++cb) {
+                float v[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN + cb * 32),
+                          v);
+                const int col0 = n0 + cb * 32;
+                const int nvalid = min(32, a.V - col0);
+                if (!live || nvalid <= 0) continue;
+                if (kSample) {
+                    float m = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (i < nvalid) m = fmaxf(m, v[i]);
+                    if (m != -INFINITY) {
+                        const float Mn = fmaxf(Mr, m * a.c);
+                        float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (i < nvalid) sacc[i & 3] += ex2(fmaf(v[i], a.c, -Mn));
+                        Sr = Sr * ex2(Mr - Mn) + ((sacc[0] + sacc[1]) + (sacc[2] + sacc[3]));
+                        Mr = Mn;
+                    }
+                    float *dst = a.spill + static_cast<size_t>(row) * a.V + col0;
+                    if (vec_store && nvalid == 32) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4 *>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (i < nvalid) dst[i] = v[i];
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (i < nvalid && (bi == 0x7fffffff || v[i] > bv)) {
+                            bv = v[i];
+                            bi = col0 + i;
+                        }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);  // accumulator drained
+            if (live)
+                a.partials[static_cast<size_t>(row) * a.n_tiles + t] =
+                    kSample ? make_float2(Mr, Sr) : make_float2(bv, __int_as_float(bi));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Row-major bf16 matrix of `rows` x `cols` read in boxes of box_rows x 64.
+static bool encode_bf16_kmajor(CUtensorMap *map, const void *base, int rows, int cols, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct LmLayout {
+    size_t finish, partials, spill, total;
+};
+
+static inline size_t a256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+static LmLayout lm_layout(int B, int K, int V) {
+    const int M = B * (K + 1);
+    const size_t n_tiles = (static_cast<size_t>(V) + BN - 1) / BN;
+    LmLayout L;
+    size_t o = 0;
+    L.finish = o;
+    o = a256(o + finish_workspace_size(B, M, V));
+    L.partials = o;
+    o = a256(o + sizeof(float2) * static_cast<size_t>(M) * n_tiles);
+    L.spill = o;
+    o = a256(o + sizeof(float) * static_cast<size_t>(M) * V);
+    L.total = o;
+    return L;
+}
+
+template <bool kSample>
+static void launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const LmArgs &a, cudaStream_t s) {
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    const int smem = static_cast<int>(sizeof(LmSmem)) + 1024;
+    if (!configured[dev]) {
+        cudaFuncSetAttribute(lmhead_gemm_kernel<kSample>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        configured[dev] = true;
+    }
+    const int grid = a.n_tiles < sm_count() ? a.n_tiles : sm_count();
+    lmhead_gemm_kernel<kSample><<<grid, kThreadsLm, smem, s>>>(ta, tb, a);
+}
+
+}  // namespace lm
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" size_t spec_lmhead_workspace_size(int B, int K, int d, int V) {
+    (void)d;
+    if (B <= 0 || K < 0 || V <= 0) return 256;
+    return lm::lm_layout(B, K, V).total;
+}
+
+extern "C" sv_status spec_lmhead_verify(const void *hidden, const void *w_vocab_t, int d, const float *q, int B,
+                                        int K, int V, float temperature, const int32_t *draft,
+                                        const float *uniforms, int32_t *out_tokens, int32_t *accept_len,
+                                        float *diag, void *ws, size_t ws_bytes, void *stream) {
+    if (B < 0 || K < 0 || K > SV_MAX_K || V <= 0 || !(temperature >= 0.f) || !std::isfinite(temperature))
+        return SV_ERR_INVALID;
+    if (B == 0) {
+        set_launches(0);
+        return SV_OK;
+    }
+    const int M = B * (K + 1);
+    const bool sample = temperature > 0.f;
+    if (M > lm::BM || d < lm::BK || d % lm::BK != 0) return SV_ERR_INVALID;
+    if (!hidden || !w_vocab_t || !out_tokens || !accept_len || !ws) return SV_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(hidden) & 15u) || (reinterpret_cast<uintptr_t>(w_vocab_t) & 15u))
+        return SV_ERR_INVALID;
+    if (K > 0 && !draft) return SV_ERR_INVALID;
+    if (sample && (!uniforms || (K > 0 && !q))) return SV_ERR_INVALID;
+    const lm::LmLayout L = lm::lm_layout(B, K, V);
+    if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return SV_ERR_WORKSPACE;
+
+    CUtensorMap ta, tb;
+    if (!lm::encode_bf16_kmajor(&ta, hidden, M, d, lm::BM) || !lm::encode_bf16_kmajor(&tb, w_vocab_t, V, d, lm::BN))
+        return SV_ERR_CUDA;
+    char *w = static_cast<char *>(ws);
+    lm::LmArgs a;
+    a.M = M;
+    a.d = d;
+    a.V = V;
+    a.n_tiles = (V + lm::BN - 1) / lm::BN;
+    a.c = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(temperature)) : 1.f;
+    a.spill = sample ? reinterpret_cast<float *>(w + L.spill) : nullptr;
+    a.partials = reinterpret_cast<float2 *>(w + L.partials);
+    a.status = reinterpret_cast<uint32_t *>(w + L.finish);  // the status word is the workspace's first word
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    prof_begin(s);
+    if (sample) lm::launch_gemm<true>(ta, tb, a, s);
+    else lm::launch_gemm<false>(ta, tb, a, s);
+    prof_end(s);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    int more = 0;
+    const sv_status st = finish_from_partials(reinterpret_cast<const float *>(w + L.spill), a.partials, a.n_tiles, q,
+                                              B, K, V, sample ? temperature : 1.f, sample, draft, uniforms,
+                                              out_tokens, accept_len, diag, w + L.finish, L.partials - L.finish, s,
+                                              &more);
+    set_launches(1 + more);
+    return st;
 }

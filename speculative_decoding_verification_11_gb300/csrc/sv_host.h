@@ -4,10 +4,19 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/specverify.h"
+
 namespace sv {
 int sm_count();                    // SMs of the current device
 void prof_begin(cudaStream_t s);   // profiling hook around the dominant kernel
 void prof_end(cudaStream_t s);
 void set_launches(int n);          // kernels launched by the last call (this thread)
 void counter_region(int B, int rows, int V, size_t *offset, size_t *bytes);  // per-request counters
+size_t finish_workspace_size(int B, int rows, int V);
+// Decide (+ residual draw when `sample`) over fp32 logits and chunk partials
+// produced by a previous kernel on `s` (see verify.cu).
+sv_status finish_from_partials(const float *logits, const float2 *partials, int n_parts, const float *q, int B,
+                               int K, int V, float temperature, bool sample, const int32_t *draft,
+                               const float *uniforms, int32_t *out_tokens, int32_t *accept_len, float *diag,
+                               void *ws, size_t ws_bytes, cudaStream_t s, int *launches);
 }  // namespace sv

@@ -949,6 +949,18 @@ __global__ void __cluster_dims__(kResCluster, 1, 1) __launch_bounds__(kResThread
 }
 
 // ---------------------------------------------------------------------------
+// Decide step over precomputed chunk partials (the fused LM-head path writes
+// them from its GEMM epilogue): one warp per request.
+// ---------------------------------------------------------------------------
+template <bool kSample>
+__global__ void __launch_bounds__(kThreads) decide_kernel(Args a) {
+    pdl_wait_prior_grid();  // partials and logits come from the previous kernel
+    pdl_launch_dependents();
+    const int b = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (b < a.B) decide_warp<float, kSample>(a, b, threadIdx.x & 31);
+}
+
+// ---------------------------------------------------------------------------
 // CSR check for ragged calls (one CTA): offsets must start at 0, increase by
 // 1..SV_MAX_K+1 and end at `rows`.  A malformed CSR invalidates the call.
 // ---------------------------------------------------------------------------
@@ -985,7 +997,7 @@ static inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t
 // requests (whose counters reach into other regions) clears them first.
 constexpr int kTicketCap = 16384;
 
-static WsLayout ws_layout(int B, int rows, int V) {
+static WsLayout ws_layout(int B, int rows, int V, bool with_partials = true) {
     WsLayout L;
     const size_t n_chunks = (static_cast<size_t>(V) + chunk_elems<float>() - 1) / chunk_elems<float>();
     const size_t n_tiles = (static_cast<size_t>(V) + kTileElems - 1) / kTileElems;
@@ -994,7 +1006,7 @@ static WsLayout ws_layout(int B, int rows, int V) {
     L.csr_ok = o; o = align256(o + 16);
     L.tickets1 = o; o = align256(o + 4ull * static_cast<size_t>(B > kTicketCap ? B : kTicketCap));
     L.dec = o; o = align256(o + sizeof(Decision) * static_cast<size_t>(B));
-    L.partials = o; o = align256(o + sizeof(float2) * static_cast<size_t>(rows) * n_chunks);
+    L.partials = o; o = align256(o + (with_partials ? sizeof(float2) * static_cast<size_t>(rows) * n_chunks : 0));
     L.tile_mass = o; o = align256(o + sizeof(float) * static_cast<size_t>(B) * n_tiles);
     L.total = o;
     return L;
@@ -1153,6 +1165,71 @@ static sv_status verify_common(const void *logits, sv_dtype dt, const float *q,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dt == SV_F32) return run_typed<float>(a, sample, vec, s);
     return run_typed<__nv_bfloat16>(a, sample, vec, s);
+}
+
+
+// Workspace of finish_from_partials (the partials live elsewhere).
+size_t finish_workspace_size(int B, int rows, int V) { return ws_layout(B, rows, V, false).total; }
+
+template <typename KernelT>
+static cudaError_t launch_pdl(KernelT kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const Args &a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+// Decide + (sampling) residual draw over fp32 logits rows and per-(row, part)
+// partials that a previous kernel on `s` produced.  Launches 1 or 2 kernels.
+sv_status finish_from_partials(const float *logits, const float2 *partials, int n_parts, const float *q, int B,
+                               int K, int V, float temperature, bool sample, const int32_t *draft,
+                               const float *uniforms, int32_t *out_tokens, int32_t *accept_len, float *diag,
+                               void *ws, size_t ws_bytes, cudaStream_t s, int *launches) {
+    const int rows = B * (K + 1);
+    const WsLayout L = ws_layout(B, rows, V, false);
+    if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return SV_ERR_WORKSPACE;
+    char *w = static_cast<char *>(ws);
+    Args a{};
+    a.logits = logits;
+    a.q = q;
+    a.row_offsets = nullptr;
+    a.draft = draft;
+    a.uniforms = uniforms;
+    a.out_tokens = out_tokens;
+    a.accept_len = accept_len;
+    a.diag = sample ? diag : nullptr;
+    a.B = B;
+    a.K = K;
+    a.V = V;
+    a.rows = rows;
+    a.n_chunks = n_parts;
+    a.n_tiles = (V + kTileElems - 1) / kTileElems;
+    a.n_draft = rows - B;
+    a.c = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(temperature)) : 1.f;
+    a.status = reinterpret_cast<uint32_t *>(w + L.status);
+    a.csr_ok = nullptr;
+    a.tickets1 = reinterpret_cast<uint32_t *>(w + L.tickets1);
+    a.dec = reinterpret_cast<Decision *>(w + L.dec);
+    a.partials = const_cast<float2 *>(partials);
+    a.tile_mass = reinterpret_cast<float *>(w + L.tile_mass);
+    const dim3 grid_d((B + kWarps - 1) / kWarps);
+    cudaError_t e = sample ? launch_pdl(decide_kernel<true>, grid_d, dim3(kThreads), 0, s, a)
+                           : launch_pdl(decide_kernel<false>, grid_d, dim3(kThreads), 0, s, a);
+    if (e != cudaSuccess) return SV_ERR_CUDA;
+    *launches = 1;
+    if (sample) {
+        const bool vec = aligned16(logits) && (V % 4 == 0) && (!q || aligned16(q));
+        if (vec) launch_pass2<float, true>(a, s); else launch_pass2<float, false>(a, s);
+        *launches = 2;
+    }
+    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 }  // namespace sv

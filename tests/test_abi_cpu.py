@@ -91,6 +91,7 @@ def test_workspace_errors(lib):
 
 def test_empty_batch_is_a_no_op(lib):
     assert lib.spec_verify_greedy(FAKE, 0, 0, 3, 100, FAKE, FAKE, FAKE, ALIGNED_WS, 256, None) == binding.SV_OK
+    assert lib.spec_lmhead_workspace_size(16, 7, 8192, 128256) >= 128 * 128256 * 4
     assert lib.spec_last_launch_count() == 0
 
 
