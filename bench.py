@@ -326,6 +326,140 @@ def run_ours(args):
     return 0
 
 
+def _peak_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def run_lmhead(args):
+    """Fused LM-head + verify, B=16 K=7 (128 rows) d=8192 V=128256, T=1, plus
+    the pages' speedup closed form from measured times."""
+    import torch
+    import oracle
+    from oracle import speedup as SP
+    from speculative_decoding_verification_11_gb300 import binding as B_, build as build_mod, workloads as W
+    world, rank, local = _dist()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    build_mod.build()
+    B_.load()
+    batch = W.lmhead()
+    Bn, K, V, T = batch.B, batch.K, batch.V, batch.temperature
+    d = batch.hidden.shape[1]
+    M = batch.rows
+    h, w = batch.hidden.to(dev), batch.w_vocab_t.to(dev)
+    q, x, u = batch.q.to(dev), batch.draft.to(dev), batch.uniforms.to(dev)
+    out = torch.empty(M, dtype=torch.int32, device=dev)
+    al = torch.empty(Bn, dtype=torch.int32, device=dev)
+    ws = B_.workspace(B_.spec_lmhead_workspace_size(Bn, K, d, V), dev)
+    stream = torch.cuda.current_stream(dev)
+    # plain decoding step of the same batch: one row per request (K = 0)
+    h0 = h.view(Bn, K + 1, d)[:, 0].contiguous()
+    u0 = u.view(Bn, K + 1)[:, 0].contiguous()
+    out0 = torch.empty(Bn, dtype=torch.int32, device=dev)
+    al0 = torch.empty(Bn, dtype=torch.int32, device=dev)
+    x0 = torch.empty(0, dtype=torch.int32, device=dev)
+    ws0 = B_.workspace(B_.spec_lmhead_workspace_size(Bn, 0, d, V), dev)
+    # stand-in draft model step: the draft head GEMM at M = B (cuBLAS) + softmax
+    hd = torch.randn(Bn, 2048, device=dev).to(torch.bfloat16)
+    wd = (torch.randn(V, 2048, device=dev) * 0.02).to(torch.bfloat16)
+
+    def spec_step():
+        B_.spec_lmhead_verify(h, w, d, q, Bn, K, V, T, x, u, out, al, ws, stream=stream)
+
+    def plain_step():
+        B_.spec_lmhead_verify(h0, w, d, None, Bn, 0, V, T, x0, u0, out0, al0, ws0, stream=stream)
+
+    def draft_step():
+        torch.softmax((hd @ wd.T).float(), dim=-1)
+
+    def timed(fn, n, prof=False):
+        ts, ks = [], []
+        for i in range(n):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            for ev in e:
+                ev.record(stream)
+            if prof:
+                B_.spec_profile_set_events(e[2], e[3])
+            e[0].record(stream)
+            fn()
+            e[1].record(stream)
+            if prof:
+                B_.spec_profile_set_events(None, None)
+            torch.cuda.synchronize()
+            ts.append(e[0].elapsed_time(e[1]))
+            if prof:
+                ks.append(e[2].elapsed_time(e[3]))
+        return ts, ks
+
+    for fn in (spec_step, plain_step, draft_step):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    clocks.start()
+    ts, ks = timed(spec_step, args.steps, prof=True)
+    clk = clocks.stop()
+    ms = statistics.mean(ts)
+    kms = statistics.mean(ks)
+    t_plain = statistics.median(timed(plain_step, max(5, args.steps // 2))[0])
+    t_draft1 = statistics.median(timed(draft_step, max(5, args.steps // 2))[0])
+    al_mean = float(al.float().mean())
+    # directly timed: round(AL) plain steps against one speculative step + K draft steps
+    n_plain = max(1, int(round(al_mean)))
+
+    def plain_loop():
+        for _ in range(n_plain):
+            plain_step()
+
+    def spec_cycle():
+        for _ in range(K):
+            draft_step()
+        spec_step()
+
+    t_plain_loop = statistics.median(timed(plain_loop, 5)[0])
+    t_spec_cycle = statistics.median(timed(spec_cycle, 5)[0])
+    w_bytes = V * d * 2
+    gemm_bytes = w_bytes + M * d * 2 + M * V * 4 + M * ((V + 255) // 256) * 8
+    flops = 2.0 * M * d * V
+    peak, pk = _peaks()
+    tpk, tpk_kind = _peak_tflops()
+    achieved = gemm_bytes / (kms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": Bn * K / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 GEMM, f32 verify", "data": "synthetic",
+        "config": {"workload": "fused LM-head + verify B=16 K=7 (128 rows) d=8192 V=128256 T=1", "B": Bn,
+                   "K": K, "V": V, "d": d, "l2": "inputs 2.1 GB > L2"},
+        "roofline": {"kernel": "lmhead_gemm_kernel (tcgen05, W stream)", "bound": "hbm", "achieved": achieved,
+                     "peak": peak, "peak_kind": pk, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": _traffic("lmhead_gemm_kernel"), "algorithmic_bytes_per_launch": gemm_bytes,
+                     "ms_per_launch": kms,
+                     "tensor": {"achieved_tflops": flops / (kms * 1e-3) / 1e12, "peak_tflops": tpk,
+                                "peak_kind": tpk_kind, "frac": flops / (kms * 1e-3) / 1e12 / tpk}},
+        "speedup_model": {
+            "T_verif_B_ms": t_plain, "T_verif_B1D_ms": ms, "T_draft_ms": K * t_draft1, "AL": al_mean,
+            "closed_form": SP.measured_speedup(t_plain, ms, K * t_draft1, al_mean),
+            "direct": {"plain_steps": n_plain, "plain_loop_ms": t_plain_loop, "spec_cycle_ms": t_spec_cycle,
+                       "ratio": t_plain_loop / t_spec_cycle},
+            "draft_stand_in": "draft head GEMM (B x 2048 . 2048 x V, bf16, cuBLAS) + softmax per drafted token"},
+        "clocks": clk,
+        "gpu_launches": 3 * args.steps,
+    }
+    if not args.no_cpu:
+        t0 = time.perf_counter()
+        oracle.lmhead_verify(batch.hidden, batch.w_vocab_t, batch.q, batch.draft, batch.uniforms, Bn, K, T)
+        el = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": Bn * K / el, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"whole batch once: fp64 GEMM (numpy BLAS, all cores) + C verify, {el:.1f} s"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -333,9 +467,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--config", choices=["sampling", "lmhead"], default="sampling",
+                    help="sampling: the headline workload; lmhead: the fused LM-head front end")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.config == "lmhead":
+        return run_lmhead(args)
     return run_ours(args)
 
 

@@ -6,18 +6,20 @@
 // M = B (K+1) <= 128 rows of hidden are one tcgen05 M tile, and the kernel
 // streams W_vocab (kept as its transpose, V x d, K-major) once.
 //
-// Persistent CTA per SM over 256-wide vocabulary tiles:
-//   warp 0    TMA producer: 128 x 64 hidden tile + 256 x 64 W tile per stage
-//             (128-byte swizzle), 4-stage ring (full/empty mbarriers); W is
+// Persistent CTA per SM over BN-wide vocabulary tiles (BN in {256, 224, 192,
+// 128}, chosen per call so that the last wave of tiles is as full as possible):
+//   warp 0    TMA producer: 128 x 64 hidden tile + BN x 64 W tile per stage
+//             (128-byte swizzle), 4-6 stage ring (full/empty mbarriers); W is
 //             streamed with an evict-first L2 hint, hidden with evict-last.
 //   warp 1    TMEM allocator and single-thread MMA issuer: 4 tcgen05.mma
-//             (kind::f16, bf16 x bf16 -> fp32, M=128, N=256, K=16) per stage
-//             into one of two 256-column TMEM accumulators; tcgen05.commit
+//             (kind::f16, bf16 x bf16 -> fp32, M=128, N=BN, K=16) per stage
+//             into one of two BN-column TMEM accumulators; tcgen05.commit
 //             frees the stage and, after the last k step, publishes the tile.
-//   warps 2-5 epilogue: tcgen05.ld of the accumulator (thread = row), per row
-//             and tile the partial (M, s) = (max z c, sum 2^(z c - M)) or
-//             (max z, first argmax), and in sampling mode an fp32 copy of the
-//             tile's logits for the decide gathers and the residual draw.
+//   warps 2-5 epilogue: tcgen05.ld of the accumulator (thread = row); each
+//             row keeps one running partial (M, s) = (max z c, sum 2^(z c - M))
+//             or (max z, first argmax) over all tiles of its CTA, written once
+//             at the end, and in sampling mode an fp32 copy of the tiles'
+//             logits for the decide gathers and the residual draw.
 // The decide step and the residual draw then run over these partials and
 // logits (finish_from_partials in verify.cu).
 #include <cuda.h>
@@ -36,27 +38,32 @@ namespace sv {
 namespace lm {
 
 constexpr int BM = 128;                 // rows of the M tile (all rows of the batch)
-constexpr int BN = 256;                 // vocabulary entries per tile
 constexpr int BK = 64;                  // hidden-size slice per stage: 128 bytes of bf16
 constexpr int UK = 16;                  // K of one tcgen05.mma kind::f16
-constexpr int kStagesLm = 4;
 constexpr int kABytes = BM * BK * 2;    // 16 KB
-constexpr int kBBytes = BN * BK * 2;    // 32 KB
-constexpr int kTmemCols = 2 * BN;       // two fp32 accumulators of BN columns
 constexpr int kEpiWarps = 4;
 constexpr int kThreadsLm = (2 + kEpiWarps) * 32;
 constexpr long long kLmWaitBudget = 4000000000ll;
+constexpr int kLmSmemBudget = 204800;   // shared bytes for the operand ring
 
-// tcgen05 instruction descriptor, kind::f16: D f32, A bf16, B bf16, both
-// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
+// Vocabulary tile width BN (a multiple of 32, <= 256) and the ring depth that
+// fits the shared-memory budget.
+template <int BN> struct Tile {
+    static constexpr int kBBytes = BN * BK * 2;
+    static constexpr int kStages = (kLmSmemBudget / (kABytes + kBBytes)) < 6 ? (kLmSmemBudget / (kABytes + kBBytes)) : 6;
+    static constexpr int kTmemCols = 2 * BN <= 256 ? 256 : 512;  // two fp32 accumulators, power of two
+    // tcgen05 instruction descriptor, kind::f16: D f32, A bf16, B bf16, both
+    // K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+    static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                       (static_cast<uint32_t>(BN >> 3) << 17) |
+                                       (static_cast<uint32_t>(BM >> 4) << 24);
+};
 
-struct LmSmem {
-    alignas(1024) unsigned char a[kStagesLm][kABytes];
-    alignas(1024) unsigned char b[kStagesLm][kBBytes];
-    uint64_t full[kStagesLm];
-    uint64_t empty[kStagesLm];
+template <int BN> struct LmSmem {
+    alignas(1024) unsigned char a[Tile<BN>::kStages][kABytes];
+    alignas(1024) unsigned char b[Tile<BN>::kStages][Tile<BN>::kBBytes];
+    uint64_t full[Tile<BN>::kStages];
+    uint64_t empty[Tile<BN>::kStages];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t mma_done;
@@ -68,7 +75,7 @@ struct LmArgs {
     int M, d, V, n_tiles;
     float c;          // log2(e) / T
     float *spill;     // M x V fp32 logits (sampling), or nullptr
-    float2 *partials; // M x n_tiles
+    float2 *partials; // M x gridDim.x: one merged partial per row and CTA
     uint32_t *status;
 };
 
@@ -157,11 +164,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <bool kSample>
+template <bool kSample, int BN>
 __global__ void __launch_bounds__(kThreadsLm, 1)
     lmhead_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, LmArgs a) {
+    constexpr int kStagesLm = Tile<BN>::kStages;
+    constexpr int kBBytes = Tile<BN>::kBBytes;
+    constexpr int kTmemCols = Tile<BN>::kTmemCols;
     extern __shared__ unsigned char smem_raw[];
-    LmSmem &sm = *reinterpret_cast<LmSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    LmSmem<BN> &sm =
+        *reinterpret_cast<LmSmem<BN> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nk = a.d / BK;
     if (tid == 0) {
@@ -234,7 +245,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                     const uint64_t bd = smem_desc_sw128(sm.b[s]);
 #pragma unroll
                     for (int kk = 0; kk < BK / UK; ++kk)  // advance 32 bytes (16 bf16) inside the swizzle atom
-                        tc_mma(d_tmem, ad + 2ull * kk, bd + 2ull * kk, kIdesc, (kb | kk) ? 1u : 0u);
+                        tc_mma(d_tmem, ad + 2ull * kk, bd + 2ull * kk, Tile<BN>::kIdesc, (kb | kk) ? 1u : 0u);
                     tc_commit(&sm.empty[s]);
                 }
                 if (!ok) break;
@@ -250,6 +261,10 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
         const int row = quad * 32 + lane;
         const bool live = row < a.M;
         const bool vec_store = (a.V & 3) == 0;
+        // running partial of this row over every tile of the CTA
+        float Mr = -INFINITY, Sr = 0.f;
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
         int ti = 0;
         for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++ti) {
             const int buf = ti & 1;
@@ -257,9 +272,6 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
             if (*abort_flag) break;
             tc_fence_after();
             const int n0 = t * BN;
-            float Mr = -INFINITY, Sr = 0.f;
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
 #pragma unroll 1
             for (int cb = 0; cb < BN / 32; ++cb) {
                 float v[32];
@@ -304,10 +316,10 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);  // accumulator drained
-            if (live)
-                a.partials[static_cast<size_t>(row) * a.n_tiles + t] =
-                    kSample ? make_float2(Mr, Sr) : make_float2(bv, __int_as_float(bi));
         }
+        if (live)
+            a.partials[static_cast<size_t>(row) * gridDim.x + blockIdx.x] =
+                kSample ? make_float2(Mr, Sr) : make_float2(bv, __int_as_float(bi));
     }
     tc_fence_before();
     __syncthreads();
@@ -353,9 +365,28 @@ struct LmLayout {
 
 static inline size_t a256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Tile width that fills the last wave of tiles best (ties: the wider tile).
+static int choose_bn(int V, int sms) {
+    const int cands[4] = {256, 224, 192, 128};
+    int best = 256;
+    double best_eff = -1.0;
+    for (int bn : cands) {
+        const long long tiles = (V + bn - 1) / bn;
+        const long long waves = (tiles + sms - 1) / sms;
+        const double eff = static_cast<double>(tiles) / static_cast<double>(waves * sms);
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = bn;
+        }
+    }
+    return best;
+}
+
+constexpr int kMaxLmGrid = 1024;  // partials are sized for at most this many CTAs
+
 static LmLayout lm_layout(int B, int K, int V) {
     const int M = B * (K + 1);
-    const size_t n_tiles = (static_cast<size_t>(V) + BN - 1) / BN;
+    const size_t n_tiles = kMaxLmGrid;  // one partial per row and CTA
     LmLayout L;
     size_t o = 0;
     L.finish = o;
@@ -368,19 +399,30 @@ static LmLayout lm_layout(int B, int K, int V) {
     return L;
 }
 
-template <bool kSample>
-static void launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const LmArgs &a, cudaStream_t s) {
+// Launch with `grid` CTAs (grid <= n_tiles, <= kMaxLmGrid).
+template <bool kSample, int BN>
+static void launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const LmArgs &a, int grid, cudaStream_t s) {
     static bool configured[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
-    const int smem = static_cast<int>(sizeof(LmSmem)) + 1024;
+    const int smem = static_cast<int>(sizeof(LmSmem<BN>)) + 1024;
     if (!configured[dev]) {
-        cudaFuncSetAttribute(lmhead_gemm_kernel<kSample>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(lmhead_gemm_kernel<kSample, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         configured[dev] = true;
     }
-    const int grid = a.n_tiles < sm_count() ? a.n_tiles : sm_count();
-    lmhead_gemm_kernel<kSample><<<grid, kThreadsLm, smem, s>>>(ta, tb, a);
+    lmhead_gemm_kernel<kSample, BN><<<grid, kThreadsLm, smem, s>>>(ta, tb, a);
+}
+
+template <bool kSample>
+static void launch_gemm_bn(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const LmArgs &a, int grid,
+                           cudaStream_t s) {
+    switch (bn) {
+        case 224: launch_gemm<kSample, 224>(ta, tb, a, grid, s); break;
+        case 192: launch_gemm<kSample, 192>(ta, tb, a, grid, s); break;
+        case 128: launch_gemm<kSample, 128>(ta, tb, a, grid, s); break;
+        default: launch_gemm<kSample, 256>(ta, tb, a, grid, s); break;
+    }
 }
 
 }  // namespace lm
@@ -415,27 +457,31 @@ extern "C" sv_status spec_lmhead_verify(const void *hidden, const void *w_vocab_
     const lm::LmLayout L = lm::lm_layout(B, K, V);
     if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return SV_ERR_WORKSPACE;
 
+    const int bn = lm::choose_bn(V, sm_count());
+    const int n_tiles = (V + bn - 1) / bn;
+    int grid = n_tiles < sm_count() ? n_tiles : sm_count();
+    if (grid > lm::kMaxLmGrid) grid = lm::kMaxLmGrid;
     CUtensorMap ta, tb;
-    if (!lm::encode_bf16_kmajor(&ta, hidden, M, d, lm::BM) || !lm::encode_bf16_kmajor(&tb, w_vocab_t, V, d, lm::BN))
+    if (!lm::encode_bf16_kmajor(&ta, hidden, M, d, lm::BM) || !lm::encode_bf16_kmajor(&tb, w_vocab_t, V, d, bn))
         return SV_ERR_CUDA;
     char *w = static_cast<char *>(ws);
     lm::LmArgs a;
     a.M = M;
     a.d = d;
     a.V = V;
-    a.n_tiles = (V + lm::BN - 1) / lm::BN;
+    a.n_tiles = n_tiles;
     a.c = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(temperature)) : 1.f;
     a.spill = sample ? reinterpret_cast<float *>(w + L.spill) : nullptr;
     a.partials = reinterpret_cast<float2 *>(w + L.partials);
     a.status = reinterpret_cast<uint32_t *>(w + L.finish);  // the status word is the workspace's first word
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     prof_begin(s);
-    if (sample) lm::launch_gemm<true>(ta, tb, a, s);
-    else lm::launch_gemm<false>(ta, tb, a, s);
+    if (sample) lm::launch_gemm_bn<true>(bn, ta, tb, a, grid, s);
+    else lm::launch_gemm_bn<false>(bn, ta, tb, a, grid, s);
     prof_end(s);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
     int more = 0;
-    const sv_status st = finish_from_partials(reinterpret_cast<const float *>(w + L.spill), a.partials, a.n_tiles, q,
+    const sv_status st = finish_from_partials(reinterpret_cast<const float *>(w + L.spill), a.partials, grid, q,
                                               B, K, V, sample ? temperature : 1.f, sample, draft, uniforms,
                                               out_tokens, accept_len, diag, w + L.finish, L.partials - L.finish, s,
                                               &more);

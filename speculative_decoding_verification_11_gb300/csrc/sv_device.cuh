@@ -173,6 +173,12 @@ namespace sv {
 // ---------------------------------------------------------------------------
 // Thread-block cluster primitives
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

@@ -10,7 +10,7 @@
 //         the decide step in one warp: accept tests u q(x) <= p(x), ballot
 //         for the first rejection, emitted drafts, AL, and the record of the
 //         row the final token comes from.
-// Pass 2  residual_kernel (sampling only) one 2-CTA cluster per request over
+// Pass 2  residual_kernel (sampling only) one cluster of 1-8 CTAs per request over
 //         the selected row, one warp per 1024-token tile: r = max(0, p - q)
 //         at a rejection or r = p for the bonus, tile masses in shared
 //         memory; rank 0 takes the prefix over tiles in fp64 through
@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(kThreads) stats_scalar_kernel(Args a) {
 
 // ---------------------------------------------------------------------------
 // Pass 2: residual masses per 1024-token tile and the inverse-CDF draw.
-// One thread-block cluster of kResCluster CTAs per request splits the
+// One thread-block cluster of C CTAs per request splits the
 // selected row's tiles; tile masses stay in each CTA's shared memory.  After a
 // cluster barrier, warp 0 of rank 0 reads all masses through distributed
 // shared memory, takes the prefix over tiles in fp64 and resolves the token.
@@ -630,7 +630,7 @@ __global__ void __launch_bounds__(kThreads) stats_scalar_kernel(Args a) {
 // tile's running sums short of u R, the draw moves on to the next token with
 // r > 0, which is what the exact inverse CDF gives up to that rounding.
 // ---------------------------------------------------------------------------
-constexpr int kResCluster = 2;
+constexpr int kMaxResCluster = 8;  // portable cluster size limit
 constexpr int kResWarps = 16;
 constexpr int kResThreads = kResWarps * 32;
 
@@ -924,18 +924,19 @@ __device__ __forceinline__ void draw_final(const Args &a, int b, const Decision 
 }
 
 template <typename T, bool kVecPath>
-__global__ void __cluster_dims__(kResCluster, 1, 1) __launch_bounds__(kResThreads, 1) residual_kernel(Args a) {
-    extern __shared__ float smass[];  // ceil(n_tiles / kResCluster) tile masses of this CTA
+__global__ void __launch_bounds__(kResThreads, 1) residual_kernel(Args a) {
+    extern __shared__ float smass[];  // ceil(n_tiles / cluster size) tile masses of this CTA
     pdl_wait_prior_grid();  // decisions come from pass 1
     if (a.csr_ok && !__ldcg(a.csr_ok)) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
-    const int b = blockIdx.x / kResCluster;
+    const int csize = static_cast<int>(cluster_nctarank());
+    const int b = blockIdx.x / csize;
     const Decision d = a.dec[b];
     if (!d.valid) return;  // same decision for every CTA of the cluster
     const T *zrow = reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(d.row) * a.V;
     const float *qrow = (d.qrow >= 0) ? a.q + static_cast<size_t>(d.qrow) * a.V : nullptr;
-    const int per = (a.n_tiles + kResCluster - 1) / kResCluster;
+    const int per = (a.n_tiles + csize - 1) / csize;
     const int t0 = static_cast<int>(rank) * per;
     const int t1 = min(t0 + per, a.n_tiles);
     for (int t = t0 + warp; t < t1; t += kResWarps) {
@@ -1068,21 +1069,29 @@ static void launch_scalar_pass1(const Args &a, cudaStream_t s) {
     stats_scalar_kernel<T, kSample><<<grid, kThreads, 0, s>>>(a);
 }
 
-// Pass 2 is launched as a programmatic dependent of pass 1: its CTAs may be
-// scheduled while pass 1 drains and wait (griddepcontrol.wait) for pass 1's
-// completion before reading the decisions.
+// Pass 2 runs one cluster of C CTAs per request, C the largest power of two
+// <= 8 that keeps B C within one CTA per SM.  It is launched as a
+// programmatic dependent of pass 1: its CTAs may be scheduled while pass 1
+// drains and wait (griddepcontrol.wait) for pass 1's completion before
+// reading the decisions.
 template <typename T, bool kVecPath>
 static void launch_pass2(const Args &a, cudaStream_t s) {
+    int C = 1;
+    while (C < kMaxResCluster && static_cast<long long>(a.B) * (2 * C) <= sm_count()) C *= 2;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.B) * kResCluster);
+    cfg.gridDim = dim3(static_cast<unsigned>(a.B) * static_cast<unsigned>(C));
     cfg.blockDim = dim3(kResThreads);
-    cfg.dynamicSmemBytes = sizeof(float) * static_cast<size_t>((a.n_tiles + kResCluster - 1) / kResCluster);
+    cfg.dynamicSmemBytes = sizeof(float) * static_cast<size_t>((a.n_tiles + C - 1) / C);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(C);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaLaunchKernelEx(&cfg, residual_kernel<T, kVecPath>, a);
 }
 
