@@ -309,9 +309,9 @@ def run_ours(args):
         "step_gbs_algorithmic": step_alg / (ms * 1e-3) / 1e9,
         "mean_accept_len": float(al_h.float().mean()),
         "emitted_tokens_per_s": world * float(al_h.sum()) / (ms * 1e-3),
-        "roofline": {"kernel": "stats_decide_kernel (logits stream)", "bound": "hbm",
+        "roofline": {"kernel": "stats_tma_kernel (logits stream)", "bound": "hbm",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": _traffic("stats_decide_kernel"),
+                     "frac": achieved / peak, "traffic": _traffic("stats_tma_kernel"),
                      "algorithmic_bytes_per_launch": pass1_alg, "ms_per_launch": kms},
         "cpu_baseline": cpu,
         "e2e": {"value": world * units / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
