@@ -12,6 +12,10 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kLoadsPerThread = 8;     // 16-byte loads in flight per thread per chunk
 constexpr int kTileElems = kThreads * 4;  // residual tile: 4 tokens per thread
 constexpr int kMaxRowsPerRequest = 256;   // SV_MAX_K + 1
+constexpr int kSegElems = 256;            // fused kernel: residual masses are kept per 256-token segment
+constexpr int kResStageElems = 4096;      // fused kernel: tokens of one residual ring stage
+constexpr int kResBlockStages = 1;        // fused kernel: stages per residual work block
+constexpr int kResBlockElems = kResStageElems * kResBlockStages;
 
 // Elements per 16-byte vector and per stats chunk for each logits type.
 template <typename T> struct Elem;
@@ -133,6 +137,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking probe of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_addr(bar)), "r"(parity)
         : "memory");

@@ -1,22 +1,20 @@
 // Verification kernels and the C ABI of libspecverify.so (sm_103a).
 //
-// Pass 1  stats_tma_kernel (rows 16-byte aligned) / stats_scalar_kernel (any)
-//         streams every logit once and reduces each 32 KB chunk of a row to
-//         (M, s) = (max z c, sum 2^(z c - M)) with c = log2(e)/T (sampling) or
-//         to (max z, first argmax) (greedy).  The TMA variant is persistent:
-//         one CTA per SM, a producer warp feeding a 6-stage shared ring with
-//         bulk async copies, 8 consumer warps that need no block barrier.
-//         The arrival that completes a request's count (release atomic) runs
-//         the decide step in one warp: accept tests u q(x) <= p(x), ballot
-//         for the first rejection, emitted drafts, AL, and the record of the
-//         row the final token comes from.
+// Rows 16-byte aligned: fused_kernel runs the whole step in one persistent
+//   kernel (see the section "Fused verification" below).
+// Any alignment: two passes.
+// Pass 1  stats_scalar_kernel: one CTA per (row, 32 KB chunk) reduces the chunk
+//         to (M, s) = (max z c, sum 2^(z c - M)) with c = log2(e)/T (sampling)
+//         or to (max z, first argmax) (greedy); the arrival that completes a
+//         request's count (release atomic) runs the decide step in one warp:
+//         accept tests u q(x) <= p(x), ballot for the first rejection, emitted
+//         drafts, AL, and the record of the row the final token comes from.
 // Pass 2  residual_kernel (sampling only) one cluster of 1-8 CTAs per request over
 //         the selected row, one warp per 1024-token tile: r = max(0, p - q)
 //         at a rejection or r = p for the bonus, tile masses in shared
 //         memory; rank 0 takes the prefix over tiles in fp64 through
 //         distributed shared memory, finds the tile holding u R, and resolves
-//         the token inside it with the same warp scan that produced the
-//         tile's mass.
+//         the token inside it with running sums in token order.
 //
 // The operation is the one stated on "Speculative Decoding in Large Language
 // Models", section 2 "Modified Rejection Sampling" (accept test, residual
@@ -62,12 +60,38 @@ struct Args {
     uint32_t *status;
     const int *csr_ok;
     uint32_t *tickets1;
+    uint32_t *sched;     // fused kernel: [0] next stats block, [1] CTAs done, [2] next residual block
     Decision *dec;
     float2 *partials;
     float *tile_mass;
+    // fused kernel records (zero until written, zeroed again by their reader)
+    uint64_t *fpart;     // per row: one partial per stats block and consumer warp (n_pe words)
+    uint64_t *fdec;      // per request: the decision, two words
+    uint32_t *fmass;     // per request: residual mass of each 256-token segment (n_seg words)
+    int n_pe;            // partial records per row
+    int n_seg;           // 256-token segments per row
+    int n_rb;            // residual blocks per row
 };
 
 constexpr long long kWaitBudget = 4000000000ll;  // SM cycles (~2 s) before a wait gives up
+
+// A decision written by another CTA during the same kernel: read it from L2
+// (an L1 line may still hold a neighbour's older bytes).
+__device__ __forceinline__ Decision load_decision(const Decision *p) {
+    static_assert(sizeof(Decision) == 32, "decision is two 16-byte words");
+    const int4 w0 = __ldcg(reinterpret_cast<const int4 *>(p));
+    const int4 w1 = __ldcg(reinterpret_cast<const int4 *>(p) + 1);
+    Decision d;
+    d.row = w0.x;
+    d.qrow = w0.y;
+    d.slot = w0.z;
+    d.valid = w0.w;
+    d.M = __int_as_float(w1.x);
+    d.invS = __int_as_float(w1.y);
+    d.u = __int_as_float(w1.z);
+    d.pad = w1.w;
+    return d;
+}
 
 __device__ __forceinline__ void request_rows(const Args &a, int b, int &r0, int &nr) {
     if (a.row_offsets) {
@@ -303,60 +327,21 @@ __device__ __forceinline__ void publish_partial(const Args &a, int row, int chun
     if (islast) decide_warp<T, kSample>(a, b, lane);
 }
 
-// ---------------------------------------------------------------------------
-// Pass 1, aligned rows: persistent CTA per SM over a contiguous range of
-// (row, chunk) items.
-//   warp 16 (producer)  streams 32 KB chunks with bulk async copies into a
-//                       kStages-deep shared ring (full/empty mbarriers);
-//   warps 0-15 (consumers) each reduce a 2 KB slice of every chunk into a
-//                       per-lane running partial of the current row segment;
-//                       at a row boundary each posts its warp partial to a
-//                       mailbox slot (mbarrier, 16 arrivals) and goes on;
-//   warp 17 (publisher) merges the 16 posts in warp order, writes the
-//                       segment's chunk partials, adds the segment's chunk
-//                       count to the request's counter (release atomic) and,
-//                       on the arrival that completes the count, runs the
-//                       decide step.
-// Consumers never wait on global memory or on each other.
-// ---------------------------------------------------------------------------
-constexpr int kStages = 6;
-constexpr int kChunkBytes = 32768;
-constexpr int kConsumerWarps = 16;
-constexpr int kTmaVecs = kChunkBytes / 16 / (kConsumerWarps * 32);  // 16-byte vectors per lane per chunk
-constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kPublisherWarp = kConsumerWarps + 1;
-constexpr int kTmaThreads = (kConsumerWarps + 2) * 32;
-constexpr int kSegSlots = 4;
-
-struct SegMsg {
-    int row, first_chunk, n_chunk, pad;
-};
-
-struct TmaSmem {
-    alignas(128) unsigned char ring[kStages][kChunkBytes];
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t seg_full[kSegSlots];
-    uint64_t seg_empty[kSegSlots];
-    float2 segpart[kSegSlots][kConsumerWarps];
-    SegMsg seg[kSegSlots];
-    int abort;
-};
-
 // Fold one chunk slice into the lane's running partial.  Vector j (VEC
 // consecutive tokens) is valid iff e0[j] < n (n is a multiple of VEC on this
-// path).  Max and sum run as trees over independent per-vector values.
-template <bool kSample, int NV, int VEC>
+// path; kFull: the whole chunk, no test).  Max and sum run as trees over
+// independent values; the exponent arguments and sums use packed fp32x2.
+template <bool kSample, bool kFull, int NV, int VEC>
 __device__ __forceinline__ void lane_accumulate(const float (&vals)[NV][VEC], const int (&e0)[NV], int n, int c0,
                                                 float c, float &ra, int &rb) {
     if (kSample) {
         float vm[NV];
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
-            float m = vals[j][0];
+            float m = fmaxf(vals[j][0], vals[j][1]);
 #pragma unroll
-            for (int k = 1; k < VEC; ++k) m = fmaxf(m, vals[j][k]);
-            vm[j] = (e0[j] < n) ? m : -INFINITY;
+            for (int k = 2; k < VEC; ++k) m = fmaxf(m, vals[j][k]);
+            vm[j] = (kFull || e0[j] < n) ? m : -INFINITY;
         }
 #pragma unroll
         for (int w = 1; w < NV; w <<= 1)
@@ -365,25 +350,25 @@ __device__ __forceinline__ void lane_accumulate(const float (&vals)[NV][VEC], co
         const float bm = vm[0];
         if (bm != -INFINITY) {
             const float Mn = fmaxf(ra, bm * c);
-            float acc[NV];
+            const float2 cc = make_float2(c, c), nm = make_float2(-Mn, -Mn);
+            float2 acc[NV];
 #pragma unroll
             for (int j = 0; j < NV; ++j) {
-                float e[VEC];
+                float2 sj = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int k = 0; k < VEC; ++k) e[k] = ex2(fmaf(vals[j][k], c, -Mn));
-#pragma unroll
-                for (int w = 1; w < VEC; w <<= 1)
-#pragma unroll
-                    for (int k = 0; k + w < VEC; k += 2 * w) e[k] += e[k + w];
-                acc[j] = (e0[j] < n) ? e[0] : 0.f;
+                for (int k = 0; k < VEC; k += 2) {
+                    const float2 y = __ffma2_rn(make_float2(vals[j][k], vals[j][k + 1]), cc, nm);
+                    sj = __fadd2_rn(sj, make_float2(ex2(y.x), ex2(y.y)));
+                }
+                acc[j] = (kFull || e0[j] < n) ? sj : make_float2(0.f, 0.f);
             }
 #pragma unroll
             for (int w = 1; w < NV; w <<= 1)
 #pragma unroll
-                for (int j = 0; j + w < NV; j += 2 * w) acc[j] += acc[j + w];
+                for (int j = 0; j + w < NV; j += 2 * w) acc[j] = __fadd2_rn(acc[j], acc[j + w]);
             const float s_old = __int_as_float(rb) * ex2(ra - Mn);  // ra = -inf: 0
             ra = Mn;
-            rb = __float_as_int(s_old + acc[0]);
+            rb = __float_as_int(s_old + (acc[0].x + acc[0].y));
         }
     } else {
         float vv[NV];
@@ -398,8 +383,9 @@ __device__ __forceinline__ void lane_accumulate(const float (&vals)[NV][VEC], co
                     m = vals[j][k];
                     mi = k;
                 }
-            vv[j] = (e0[j] < n) ? m : -INFINITY;
-            vi[j] = (e0[j] < n) ? c0 + e0[j] + mi : 0x7fffffff;
+            const bool ok = kFull || e0[j] < n;
+            vv[j] = ok ? m : -INFINITY;
+            vi[j] = ok ? c0 + e0[j] + mi : 0x7fffffff;
         }
 #pragma unroll
         for (int w = 1; w < NV; w <<= 1)
@@ -413,163 +399,6 @@ template <bool kSample>
 __device__ __forceinline__ void partial_identity(float &ra, int &rb) {
     ra = -INFINITY;
     rb = kSample ? __float_as_int(0.f) : 0x7fffffff;
-}
-
-template <typename T, bool kSample>
-__global__ void __launch_bounds__(kTmaThreads, 1) stats_tma_kernel(Args a) {
-    constexpr int VEC = Elem<T>::kVec;
-    constexpr int CHUNK = chunk_elems<T>();
-    static_assert(CHUNK * sizeof(T) == kChunkBytes, "chunk must fill one ring stage");
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    TmaSmem &sm = *reinterpret_cast<TmaSmem *>(smem_raw);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    pdl_launch_dependents();  // pass 2 may be scheduled as this grid drains
-    if (a.csr_ok && !__ldcg(a.csr_ok)) return;
-    const long long total = static_cast<long long>(a.rows) * a.n_chunks;
-    const int i0 = static_cast<int>(total * blockIdx.x / gridDim.x);
-    const int i1 = static_cast<int>(total * (blockIdx.x + 1) / gridDim.x);
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], kConsumerWarps);
-        }
-        for (int s = 0; s < kSegSlots; ++s) {
-            mbar_init(&sm.seg_full[s], kConsumerWarps);
-            mbar_init(&sm.seg_empty[s], 1);
-        }
-        sm.abort = 0;
-        fence_mbar_init();
-    }
-    __syncthreads();
-    volatile int *abort_flag = &sm.abort;
-    auto timeout = [&]() {
-        *abort_flag = 1;
-        atomicOr(a.status, SV_FLAG_TIMEOUT);
-    };
-
-    if (warp == kProducerWarp) {
-        if (lane == 0) {
-            int k = 0;
-            for (int item = i0; item < i1; ++item, ++k) {
-                const int s = k % kStages;
-                if (k >= kStages && !mbar_wait_bounded(&sm.empty[s], ((k / kStages) - 1) & 1, kWaitBudget))
-                    timeout();
-                if (*abort_flag) {
-                    // let the copies already issued into the ring land before leaving
-                    for (int kk = max(0, k - kStages); kk < k; ++kk)
-                        mbar_wait_bounded(&sm.full[kk % kStages], (kk / kStages) & 1, kWaitBudget);
-                    break;
-                }
-                const int row = item / a.n_chunks;
-                const int chunk = item - row * a.n_chunks;
-                const int c0 = chunk * CHUNK;
-                const int n = min(CHUNK, a.V - c0);
-                const T *src = reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(row) * a.V + c0;
-                const uint32_t bytes = static_cast<uint32_t>(n) * sizeof(T);
-                mbar_arrive_expect_tx(&sm.full[s], bytes);
-                bulk_g2s(sm.ring[s], src, bytes, &sm.full[s]);
-            }
-        }
-        return;
-    }
-
-    if (warp == kPublisherWarp) {
-        const int n_seg = (i1 - 1) / a.n_chunks - i0 / a.n_chunks + 1;
-        for (int g = 0; g < n_seg; ++g) {
-            const int slot = g % kSegSlots;
-            if (!mbar_wait_bounded(&sm.seg_full[slot], (g / kSegSlots) & 1, kWaitBudget)) timeout();
-            if (*abort_flag) break;
-            const SegMsg msg = sm.seg[slot];
-            float ra = -INFINITY;
-            int rb = kSample ? __float_as_int(0.f) : 0x7fffffff;
-            if (lane == 0)
-                for (int w = 0; w < kConsumerWarps; ++w) merge_pair<kSample>(ra, rb, sm.segpart[slot][w]);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.seg_empty[slot]);
-            // the segment's chunk partials: the merged value in its first chunk,
-            // the identity in the others
-            float2 *P = a.partials + static_cast<size_t>(msg.row) * a.n_chunks + msg.first_chunk;
-            for (int c = lane; c < msg.n_chunk; c += 32) {
-                float ia;
-                int ib;
-                partial_identity<kSample>(ia, ib);
-                P[c] = (c == 0) ? make_float2(ra, __int_as_float(rb)) : make_float2(ia, __int_as_float(ib));
-            }
-            __threadfence();
-            __syncwarp();
-            int islast = 0, b = 0;
-            if (lane == 0) {
-                b = request_of_row(a, msg.row);
-                int r0, nr;
-                request_rows(a, b, r0, nr);
-                const uint32_t old = atom_add_release_gpu(a.tickets1 + b, static_cast<uint32_t>(msg.n_chunk));
-                islast = (old + msg.n_chunk == static_cast<uint32_t>(nr) * static_cast<uint32_t>(a.n_chunks));
-                if (islast) fence_acq_rel_gpu();
-            }
-            islast = __shfl_sync(0xffffffffu, islast, 0);
-            b = __shfl_sync(0xffffffffu, b, 0);
-            if (islast) decide_warp<T, kSample>(a, b, lane);
-        }
-        return;
-    }
-
-    // consumers
-    int k = 0, g = 0;
-    int seg_row = i0 / a.n_chunks;
-    int seg_first = i0 - seg_row * a.n_chunks;
-    int seg_n = 0;
-    float ra;
-    int rb;
-    partial_identity<kSample>(ra, rb);
-    auto post = [&]() -> bool {
-        float wa = ra;
-        int wb = rb;
-        warp_partial_reduce<kSample>(wa, wb);
-        const int slot = g % kSegSlots;
-        if (g >= kSegSlots && !mbar_wait_bounded(&sm.seg_empty[slot], ((g / kSegSlots) - 1) & 1, kWaitBudget))
-            timeout();
-        if (*abort_flag) return false;
-        if (lane == 0) {
-            sm.segpart[slot][warp] = make_float2(wa, __int_as_float(wb));
-            if (warp == 0) sm.seg[slot] = SegMsg{seg_row, seg_first, seg_n, 0};
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.seg_full[slot]);
-        ++g;
-        return true;
-    };
-    for (int item = i0; item < i1; ++item, ++k) {
-        const int row = item / a.n_chunks;
-        const int chunk = item - row * a.n_chunks;
-        if (row != seg_row) {
-            if (!post()) return;
-            seg_row = row;
-            seg_first = chunk;
-            seg_n = 0;
-            partial_identity<kSample>(ra, rb);
-        }
-        const int s = k % kStages;
-        if (!mbar_wait_bounded(&sm.full[s], (k / kStages) & 1, kWaitBudget)) timeout();
-        if (*abort_flag) return;
-        const int c0 = chunk * CHUNK;
-        const int n = min(CHUNK, a.V - c0);
-        const uint4 *stage = reinterpret_cast<const uint4 *>(sm.ring[s]);
-        float vals[kTmaVecs][VEC];
-        int e0[kTmaVecs];
-#pragma unroll
-        for (int j = 0; j < kTmaVecs; ++j) {
-            const int v = warp * (kTmaVecs * 32) + j * 32 + lane;
-            e0[j] = v * VEC;
-            uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-            if (e0[j] < n) raw = stage[v];
-            unpack(raw, vals[j]);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[s]);  // slice consumed: the stage may be refilled
-        lane_accumulate<kSample, kTmaVecs, VEC>(vals, e0, n, c0, a.c, ra, rb);
-        ++seg_n;
-    }
-    post();
 }
 
 // ---------------------------------------------------------------------------
@@ -932,7 +761,7 @@ __global__ void __launch_bounds__(kResThreads, 1) residual_kernel(Args a) {
     const uint32_t rank = cluster_ctarank();
     const int csize = static_cast<int>(cluster_nctarank());
     const int b = blockIdx.x / csize;
-    const Decision d = a.dec[b];
+    const Decision d = load_decision(a.dec + b);
     if (!d.valid) return;  // same decision for every CTA of the cluster
     const T *zrow = reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(d.row) * a.V;
     const float *qrow = (d.qrow >= 0) ? a.q + static_cast<size_t>(d.qrow) * a.V : nullptr;
@@ -948,6 +777,841 @@ __global__ void __launch_bounds__(kResThreads, 1) residual_kernel(Args a) {
     if (rank == 0 && warp == 0) draw_final<T, kVecPath>(a, b, d, lane, smass, per);
     cluster_sync();  // every CTA's shared memory stays alive until rank 0 has read it
 }
+
+// ---------------------------------------------------------------------------
+// Fused verification: one persistent kernel runs the whole step (rows 16-byte
+// aligned).  One CTA per SM, three roles:
+//   producer (one thread)  streams 32 KB stages into a 6-stage shared-memory
+//                          ring with bulk copies: first stats blocks (4
+//                          chunks of one row) from a grid-wide counter in row
+//                          order, then residual blocks (4096 tokens of a
+//                          request's selected row and its q row) from a second
+//                          counter in request-major order, each once its
+//                          request's decision is published.  Stats go first
+//                          because every decision waits on them, and a
+//                          residual stage queued ahead of them in a ring would
+//                          delay the decisions still to come;
+//   16 consumer warps      reduce each stats block to one partial per warp
+//                          and each residual stage to one mass per 256-token
+//                          segment, and store them to the workspace;
+//   worker warp            owns requests b = CTA, CTA + G, ...: gathers the
+//                          drafts' z(x), q(x) and uniforms, waits for the
+//                          request's partials, runs the accept tests and the
+//                          first-reject scan, publishes the decision, waits
+//                          for the segment masses and draws the final token.
+// Every record that crosses CTAs is one 32- or 64-bit word that reads zero
+// until it is written (the stored encodings are never zero).  Readers poll
+// with relaxed loads and zero what they consumed, so no fence lies on a
+// request's path, and a completed call leaves the records zeroed for the
+// next one.  The arithmetic of the final draw's prefix sums is double-single
+// fp32, not fp64 (see DS below).
+// ---------------------------------------------------------------------------
+namespace fz {
+
+constexpr int kStages = 6;
+constexpr int kChunkBytes = 32768;
+constexpr int kCons = 16;                                   // consumer warps
+constexpr int kVecs = kChunkBytes / 16 / (kCons * 32);      // 16-byte vectors per lane per stats chunk
+constexpr int kProducer = kCons, kWorker = kCons + 1;
+constexpr int kThreads = (kCons + 2) * 32;
+constexpr int kBlockChunks = 4;                             // chunks per stats block
+constexpr int kResElems = kResStageElems;                   // tokens per residual stage
+constexpr int kResQOffset = 16384;                          // byte offset of the q part in a stage
+constexpr unsigned kPollNs = 64;
+
+enum { kStats = 0, kRes = 1, kEnd = 2 };
+
+struct Tag {
+    int kind;
+    int row;    // stats: logits row        residual: request
+    int chunk;  // stats: chunk index       residual: stage index within the row
+    int n;      // tokens in the stage
+    int has_q;  // residual: 1 if the q part is present
+    int last;   // stats: 1 on the block's last chunk
+    float M, invS;  // residual: the decision's normaliser
+};
+
+struct Smem {
+    alignas(128) unsigned char ring[kStages][kChunkBytes];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    Tag tag[kStages];
+    int abort;
+};
+
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t *p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(uint64_t *p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_u32(uint32_t *p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// A partial (a, b) as one word: low half a; high half b with its top bit
+// flipped.  b is a sum of exponentials (>= +0) or a token index (>= 0), so
+// the high half is never zero.
+template <bool kSample>
+__device__ __forceinline__ uint64_t enc_partial(float a, int b) {
+    if (kSample) b = __float_as_int(__fadd_rn(__int_as_float(b), 0.f));  // -0 -> +0
+    return (static_cast<uint64_t>(static_cast<uint32_t>(b) ^ 0x80000000u) << 32) | __float_as_uint(a);
+}
+__device__ __forceinline__ bool partial_written(uint64_t w) { return (w >> 32) != 0; }
+__device__ __forceinline__ float2 dec_partial(uint64_t w) {
+    return make_float2(__uint_as_float(static_cast<uint32_t>(w)),
+                       __int_as_float(static_cast<int>(static_cast<uint32_t>(w >> 32) ^ 0x80000000u)));
+}
+
+// A residual mass (>= 0, or NaN on bad inputs) with its top bit flipped: never zero.
+__device__ __forceinline__ uint32_t enc_mass(float m) { return __float_as_uint(__fadd_rn(m, 0.f)) ^ 0x80000000u; }
+__device__ __forceinline__ float dec_mass(uint32_t w) { return __uint_as_float(w ^ 0x80000000u); }
+
+// The decision of request b as two words: {M, 1/S} and {row, qrow + 2};
+// row < 0 marks a request without a draw (an invalid draft).
+__device__ __forceinline__ void publish_decision(uint64_t *rec, float M, float invS, int row, int qrow) {
+    st_relaxed_u64(rec, (static_cast<uint64_t>(__float_as_uint(invS) ^ 0x80000000u) << 32) | __float_as_uint(M));
+    st_relaxed_u64(rec + 1, (static_cast<uint64_t>(static_cast<uint32_t>(qrow + 2)) << 32) |
+                                static_cast<uint32_t>(row));
+}
+
+// r(v) of 8 tokens of a residual chunk held by one lane: token
+// base + (j * 32 + lane) * 4 + k of the chunk, j < 2, k < 4.
+template <typename T>
+__device__ __forceinline__ float res_lane_sum(const unsigned char *stage, int warp, int lane, int n, bool has_q,
+                                              float c, float M, float invS) {
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int v = warp * 64 + j * 32 + lane;  // index of this lane's 4-token group
+        const int e0 = v * 4;
+        if (e0 >= n) continue;
+        float z[4], qv[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (sizeof(T) == 4) {
+            const float4 w = reinterpret_cast<const float4 *>(stage)[v];
+            z[0] = w.x; z[1] = w.y; z[2] = w.z; z[3] = w.w;
+        } else {
+            const uint2 w = reinterpret_cast<const uint2 *>(stage)[v];
+            z[0] = __uint_as_float(w.x << 16);
+            z[1] = __uint_as_float(w.x & 0xffff0000u);
+            z[2] = __uint_as_float(w.y << 16);
+            z[3] = __uint_as_float(w.y & 0xffff0000u);
+        }
+        if (has_q) {
+            const float4 w = reinterpret_cast<const float4 *>(stage + kResQOffset)[v];
+            qv[0] = w.x; qv[1] = w.y; qv[2] = w.z; qv[3] = w.w;
+        }
+        float r[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float p = __fmul_rn(ex2(__fmaf_rn(z[k], c, -M)), invS);
+            r[k] = has_q ? fmaxf(__fsub_rn(p, qv[k]), 0.f) : p;
+        }
+        acc += (r[0] + r[1]) + (r[2] + r[3]);  // n is a multiple of 4 on this path
+    }
+    return acc;
+}
+
+// r(v) of the 8 tokens a lane holds in 256-token segment g of a row: token
+// g * 256 + (j * 32 + lane) * 4 + k, j < 2, k < 4; zero beyond V.  Same
+// arithmetic as res_lane_sum (V is a multiple of 4 on this path).
+template <typename T>
+__device__ __forceinline__ void seg_load_r(const T *zrow, const float *qrow, int V, int g, float c, float M,
+                                           float invS, int lane, float (&r)[2][4]) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int e0 = g * kSegElems + (j * 32 + lane) * 4;
+        float z[4] = {0.f, 0.f, 0.f, 0.f}, qv[4] = {0.f, 0.f, 0.f, 0.f};
+        const bool in = e0 < V;
+        if (in) {
+            if constexpr (sizeof(T) == 4) {
+                const float4 w = __ldcs(reinterpret_cast<const float4 *>(zrow + e0));
+                z[0] = w.x; z[1] = w.y; z[2] = w.z; z[3] = w.w;
+            } else {
+                const uint2 w = __ldcs(reinterpret_cast<const uint2 *>(zrow + e0));
+                z[0] = __uint_as_float(w.x << 16);
+                z[1] = __uint_as_float(w.x & 0xffff0000u);
+                z[2] = __uint_as_float(w.y << 16);
+                z[3] = __uint_as_float(w.y & 0xffff0000u);
+            }
+            if (qrow) {
+                const float4 w = __ldcs(reinterpret_cast<const float4 *>(qrow + e0));
+                qv[0] = w.x; qv[1] = w.y; qv[2] = w.z; qv[3] = w.w;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float p = __fmul_rn(ex2(__fmaf_rn(z[k], c, -M)), invS);
+            r[j][k] = in ? (qrow ? fmaxf(__fsub_rn(p, qv[k]), 0.f) : p) : 0.f;
+        }
+    }
+}
+
+// Double-single arithmetic: an unevaluated sum hi + lo of two fp32 values
+// (about 48 significant bits), from error-free transformations (Knuth's
+// TwoSum; the product error from one fma).  FP64 runs at a small fraction of
+// the fp32 rate on this GPU, and the draw's prefix sums sit on the critical
+// path, so they are kept in this form instead.
+struct DS {
+    float hi, lo;
+};
+__device__ __forceinline__ DS ds_two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return DS{s, e};
+}
+__device__ __forceinline__ DS ds_norm(float s, float e) {
+    const float hi = __fadd_rn(s, e);
+    return DS{hi, __fsub_rn(e, __fsub_rn(hi, s))};
+}
+__device__ __forceinline__ DS ds_add(DS a, DS b) {
+    const DS t = ds_two_sum(a.hi, b.hi);
+    return ds_norm(t.hi, __fadd_rn(t.lo, __fadd_rn(a.lo, b.lo)));
+}
+__device__ __forceinline__ DS ds_add_f(DS a, float b) {
+    const DS t = ds_two_sum(a.hi, b);
+    return ds_norm(t.hi, __fadd_rn(t.lo, a.lo));
+}
+__device__ __forceinline__ DS ds_mul_f(DS a, float b) {
+    const float p = __fmul_rn(a.hi, b);
+    const float e = __fmaf_rn(a.lo, b, __fmaf_rn(a.hi, b, -p));
+    return ds_norm(p, e);
+}
+// a > b
+__device__ __forceinline__ bool ds_gt(DS a, DS b) {
+    const DS d = ds_add(a, DS{-b.hi, -b.lo});
+    return d.hi > 0.f || (d.hi == 0.f && d.lo > 0.f);
+}
+__device__ __forceinline__ DS ds_shfl_up(DS a, int o) {
+    return DS{__shfl_up_sync(0xffffffffu, a.hi, o), __shfl_up_sync(0xffffffffu, a.lo, o)};
+}
+__device__ __forceinline__ DS ds_shfl(DS a, int src) {
+    return DS{__shfl_sync(0xffffffffu, a.hi, src), __shfl_sync(0xffffffffu, a.lo, src)};
+}
+
+// Running sums of a segment in token order (fp32 within the segment, on top
+// of the double-single prefix base_p of the segments before it): the first
+// token whose running sum passes t, or -1.
+__device__ __forceinline__ TileScan warp_seg_scan(const float (&r)[2][4], int g, int V, DS base_p, DS t, int lane) {
+    float base = 0.f;
+    TileScan res{-1, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        float pre[4];
+        pre[0] = r[j][0];
+        pre[1] = __fadd_rn(pre[0], r[j][1]);
+        pre[2] = __fadd_rn(pre[1], r[j][2]);
+        pre[3] = __fadd_rn(pre[2], r[j][3]);
+        float incl = pre[3];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl = __fadd_rn(incl, y);
+        }
+        float lex = __shfl_up_sync(0xffffffffu, incl, 1);
+        if (lane == 0) lex = 0.f;
+        const float seg = __shfl_sync(0xffffffffu, incl, 31);
+        const float head = __fadd_rn(base, lex);
+        int cand = -1;
+        const int e0 = g * kSegElems + (j * 32 + lane) * 4;
+#pragma unroll
+        for (int k = 3; k >= 0; --k)
+            if (e0 + k < V && ds_gt(ds_add_f(base_p, __fadd_rn(head, pre[k])), t)) cand = k;
+        const unsigned m = __ballot_sync(0xffffffffu, cand >= 0);
+        if (m && res.v < 0) {
+            const int src = __ffs(m) - 1;
+            const int ck = __shfl_sync(0xffffffffu, cand, src);
+            float rsel = 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (k == ck) rsel = r[j][k];
+            res.v = g * kSegElems + (j * 32 + src) * 4 + ck;
+            res.rv = __shfl_sync(0xffffffffu, rsel, src);
+        }
+        base = __fadd_rn(base, seg);
+    }
+    return res;
+}
+
+struct Sel {
+    int valid;   // 0: an invalid draft id (nothing to draw)
+    int ks;      // accepted drafts: row r0 + ks carries the final token
+    int row, qrow;
+    float M, S;  // normaliser of row ks (sampling)
+};
+
+// Lane 0's verdict, the same in every lane: stop waiting (abort or time budget spent).
+__device__ __forceinline__ bool give_up(const Args &a, volatile int *abort_flag, long long t_start, int lane) {
+    int stop = 0;
+    if (lane == 0) {
+        stop = *abort_flag;
+        if (!stop && clock64() - t_start > kWaitBudget) {
+            *abort_flag = 1;
+            atomicOr(a.status, SV_FLAG_TIMEOUT);
+            stop = 1;
+        }
+    }
+    return __shfl_sync(0xffffffffu, stop, 0) != 0;
+}
+
+// Decide step of request b by its owning worker warp.  Lane j holds row
+// jb + j: its draft's gathers go out first, then the warp waits for the rows'
+// partials (8 rows at a time, lanes over a row's partials, so every load of a
+// poll is in flight at once), merges them in index order and zeroes them.
+// Every row is consumed even after a rejection, so the records are left
+// zeroed.  Returns false when it gave up waiting.
+template <typename T, bool kSample>
+__device__ bool fused_decide(const Args &a, int b, int lane, volatile int *abort_flag, long long t_start, Sel &sel) {
+    int r0, nr;
+    request_rows(a, b, r0, nr);
+    const int Kb = nr - 1;
+    const int d0 = r0 - b;
+    const int E = a.n_pe;
+    bool bad = false;
+    for (int j = lane; j < Kb; j += 32) {
+        const int x = __ldg(a.draft + d0 + j);
+        bad |= (x < 0 || x >= a.V);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    int ks = -1;
+    float Msel = 0.f, Ssel = 1.f;
+    int argsel = 0;
+    for (int jb = 0; jb < nr; jb += 32) {
+        const int j = jb + lane;
+        int x = 0;
+        float z = 0.f, qv = 0.f, u = 0.f;
+        if (j < Kb && !bad) {
+            x = __ldg(a.draft + d0 + j);
+            if (kSample) {
+                z = logit_at<T>(a, static_cast<size_t>(r0 + j) * a.V + x);
+                qv = __ldg(a.q + static_cast<size_t>(d0 + j) * a.V + x);
+                u = __ldg(a.uniforms + r0 + j);
+            }
+        }
+        float M = -INFINITY, S = 0.f, bv = -INFINITY;
+        int bi = 0x7fffffff;
+        const int rows_here = min(32, nr - jb);
+        for (int rg = 0; rg < rows_here; rg += 8) {
+            uint64_t *base = a.fpart + static_cast<size_t>(r0 + jb + rg) * E;
+            float ma[8];
+            int mb[8];
+            for (;;) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) partial_identity<kSample>(ma[i], mb[i]);
+                bool all = true;
+                for (int e = lane; e < E; e += 32) {
+                    uint64_t w[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        w[i] = (rg + i < rows_here) ? ld_relaxed_u64(base + static_cast<size_t>(i) * E + e) : 0ull;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (rg + i < rows_here) {
+                            all &= partial_written(w[i]);
+                            merge_pair<kSample>(ma[i], mb[i], dec_partial(w[i]));
+                        }
+                }
+                if (__all_sync(0xffffffffu, all)) break;
+                if (give_up(a, abort_flag, t_start, lane)) return false;
+                __nanosleep(kPollNs);
+            }
+            for (int e = lane; e < E; e += 32)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (rg + i < rows_here) st_relaxed_u64(base + static_cast<size_t>(i) * E + e, 0ull);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                warp_partial_reduce<kSample>(ma[i], mb[i]);
+                if (lane == rg + i) {
+                    if (kSample) {
+                        M = ma[i];
+                        S = __int_as_float(mb[i]);
+                    } else {
+                        bv = ma[i];
+                        bi = mb[i];
+                    }
+                }
+            }
+        }
+        bool rej = false;
+        if (j < Kb && !bad) {
+            if (kSample) {
+                const float p = exp2f(fmaf(z, a.c, -M)) / S;
+                rej = !(u * qv <= p);
+                if (a.diag) a.diag[d0 + j] = p;
+            } else {
+                rej = (x != bi);
+            }
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, rej);
+        if (ks < 0 && !bad && (m || jb + 32 >= nr)) {
+            const int src = m ? (__ffs(m) - 1) : (Kb - jb);
+            ks = jb + src;
+            Msel = __shfl_sync(0xffffffffu, M, src);
+            Ssel = __shfl_sync(0xffffffffu, S, src);
+            argsel = __shfl_sync(0xffffffffu, bi, src);
+        }
+        (void)bv;
+    }
+    if (bad) {
+        for (int j = lane; j < nr; j += 32) a.out_tokens[r0 + j] = -1;
+        if (lane == 0) {
+            a.accept_len[b] = 0;
+            atomicOr(a.status, SV_FLAG_BAD_TOKEN);
+        }
+        sel.valid = 0;
+        sel.ks = -1;
+        sel.row = -1;
+        sel.qrow = -1;
+        return true;
+    }
+    for (int j = lane; j < nr; j += 32) {
+        int v = -1;
+        if (j < ks) v = __ldg(a.draft + d0 + j);
+        else if (j == ks && !kSample) v = argsel;
+        a.out_tokens[r0 + j] = v;
+    }
+    if (lane == 0) a.accept_len[b] = ks + 1;
+    sel.valid = 1;
+    sel.ks = ks;
+    sel.row = r0 + ks;
+    sel.qrow = (ks < Kb) ? d0 + ks : -1;
+    sel.M = Msel;
+    sel.S = Ssel;
+    return true;
+}
+
+// Sum of a segment's r(v) in a fixed order (the slow path below uses it twice).
+__device__ __forceinline__ float seg_sum(const float (&r)[2][4]) {
+    float m = ((r[0][0] + r[0][1]) + (r[0][2] + r[0][3])) + ((r[1][0] + r[1][1]) + (r[1][2] + r[1][3]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
+    return m;
+}
+
+// Final draw of request b by its owning worker warp, once every segment mass
+// of the selected row is in: an fp64 prefix over the segments, then running
+// sums in token order inside the segment that holds u R.  Rounding
+// fallbacks: sums that end short of u R take the next token with r > 0; u R
+// at or above every boundary takes the last token with r > 0.  An empty
+// residual after a rejection draws from p instead.  Returns false when it
+// gave up waiting.
+template <typename T>
+__device__ bool fused_draw(const Args &a, int b, const Sel &sel, float invS, int lane, volatile int *abort_flag,
+                           long long t_start) {
+    int r0, nr;
+    request_rows(a, b, r0, nr);
+    const T *zrow = reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(sel.row) * a.V;
+    const float *qrow = (sel.qrow >= 0) ? a.q + static_cast<size_t>(sel.qrow) * a.V : nullptr;
+    const float M = sel.M;
+    const float u = __ldg(a.uniforms + r0 + nr - 1);
+    uint32_t *mw = a.fmass + static_cast<size_t>(b) * a.n_seg;
+    const int ns = a.n_seg;
+    const int G = (ns + 31) / 32;
+    const int i0 = min(lane * G, ns), i1 = min(i0 + G, ns);
+    // this lane's masses stay in registers when they fit (V up to 131072)
+    constexpr int kRegSeg = 16;
+    const bool in_regs = G <= kRegSeg;
+    float mv[kRegSeg];
+    for (;;) {
+        bool all = true;
+        if (in_regs) {
+#pragma unroll
+            for (int i = 0; i < kRegSeg; ++i) {
+                const uint32_t w = (i0 + i < i1) ? ld_relaxed_u32(mw + i0 + i) : enc_mass(0.f);
+                all &= (w != 0u);
+                mv[i] = dec_mass(w);
+            }
+        } else {
+            for (int i = i0; i < i1; ++i) all &= (ld_relaxed_u32(mw + i) != 0u);
+        }
+        if (__all_sync(0xffffffffu, all)) break;
+        if (give_up(a, abort_flag, t_start, lane)) return false;
+        __nanosleep(kPollNs);
+    }
+    DS sum{0.f, 0.f};
+    if (in_regs) {
+#pragma unroll
+        for (int i = 0; i < kRegSeg; ++i) sum = ds_add_f(sum, mv[i]);
+    } else {
+        for (int i = i0; i < i1; ++i) sum = ds_add_f(sum, dec_mass(ld_relaxed_u32(mw + i)));
+    }
+    DS incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const DS y = ds_shfl_up(incl, o);
+        if (lane >= o) incl = ds_add(incl, y);
+    }
+    DS R = ds_shfl(incl, 31);
+    DS P = ds_shfl_up(incl, 1);
+    if (lane == 0) P = DS{0.f, 0.f};
+    DS t = ds_mul_f(R, u);
+    int found = -1;
+    DS fb{0.f, 0.f};
+    if (in_regs) {
+#pragma unroll
+        for (int i = 0; i < kRegSeg; ++i) {
+            const DS Pn = ds_add_f(P, mv[i]);
+            if (found < 0 && i0 + i < i1 && ds_gt(Pn, t)) {
+                found = i0 + i;
+                fb = P;
+            }
+            P = Pn;
+        }
+    } else {
+        for (int i = i0; i < i1; ++i) {
+            const DS Pn = ds_add_f(P, dec_mass(ld_relaxed_u32(mw + i)));
+            if (found < 0 && ds_gt(Pn, t)) {
+                found = i;
+                fb = P;
+            }
+            P = Pn;
+        }
+    }
+    for (int i = i0; i < i1; ++i) st_relaxed_u32(mw + i, 0u);  // consumed: leave the records zeroed
+    unsigned ball = __ballot_sync(0xffffffffu, found >= 0);
+    int src = ball ? (__ffs(ball) - 1) : 0;
+    int fseg = ball ? __shfl_sync(0xffffffffu, found, src) : -1;
+    DS fbase = ds_shfl(fb, src);
+    if (!(R.hi > 0.f)) {
+        // empty residual after a rejection: draw from p instead (slow path, one segment at a time)
+        qrow = nullptr;
+        if (lane == 0) atomicOr(a.status, SV_FLAG_ZERO_RESIDUAL);
+        DS acc{0.f, 0.f};
+        for (int g = 0; g < ns; ++g) {
+            float r[2][4];
+            seg_load_r<T>(zrow, nullptr, a.V, g, a.c, M, invS, lane, r);
+            acc = ds_add_f(acc, seg_sum(r));
+        }
+        R = acc;
+        t = ds_mul_f(R, u);
+        fseg = -1;
+        fbase = DS{0.f, 0.f};
+        DS Pp{0.f, 0.f};
+        for (int g = 0; g < ns && fseg < 0; ++g) {
+            float r[2][4];
+            seg_load_r<T>(zrow, nullptr, a.V, g, a.c, M, invS, lane, r);
+            const DS Pn = ds_add_f(Pp, seg_sum(r));
+            if (ds_gt(Pn, t)) {
+                fseg = g;
+                fbase = Pp;
+            }
+            Pp = Pn;
+        }
+    }
+    int vstar = -1;
+    float rstar = 0.f;
+    if (fseg >= 0) {
+        float r[2][4];
+        seg_load_r<T>(zrow, qrow, a.V, fseg, a.c, M, invS, lane, r);
+        const TileScan ts = warp_seg_scan(r, fseg, a.V, fbase, t, lane);
+        vstar = ts.v;
+        rstar = ts.rv;
+        for (int g = fseg + 1; g < ns && vstar < 0; ++g) {
+            seg_load_r<T>(zrow, qrow, a.V, g, a.c, M, invS, lane, r);
+            int loc = 0x7fffffff;
+            float rloc = 0.f;
+#pragma unroll
+            for (int j = 1; j >= 0; --j)
+#pragma unroll
+                for (int k = 3; k >= 0; --k)
+                    if (r[j][k] > 0.f) {
+                        loc = (j * 32 + lane) * 4 + k;
+                        rloc = r[j][k];
+                    }
+            const int best = __reduce_min_sync(0xffffffffu, loc);
+            if (best != 0x7fffffff) {
+                const unsigned m = __ballot_sync(0xffffffffu, loc == best);
+                rstar = __shfl_sync(0xffffffffu, rloc, __ffs(m) - 1);
+                vstar = g * kSegElems + best;
+            }
+        }
+    }
+    for (int g = ns - 1; g >= 0 && vstar < 0; --g) {
+        float r[2][4];
+        seg_load_r<T>(zrow, qrow, a.V, g, a.c, M, invS, lane, r);
+        int loc = -1;
+        float rloc = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (r[j][k] > 0.f) {
+                    loc = (j * 32 + lane) * 4 + k;
+                    rloc = r[j][k];
+                }
+        const int best = __reduce_max_sync(0xffffffffu, loc);
+        if (best >= 0) {
+            const unsigned m = __ballot_sync(0xffffffffu, loc == best);
+            rstar = __shfl_sync(0xffffffffu, rloc, __ffs(m) - 1);
+            vstar = g * kSegElems + best;
+        }
+    }
+    if (lane == 0) {
+        a.out_tokens[sel.row] = vstar;
+        if (a.diag) {
+            const float Rf = __fadd_rn(R.hi, R.lo);
+            a.diag[a.n_draft + 2 * b] = Rf;
+            a.diag[a.n_draft + 2 * b + 1] = __fdiv_rn(rstar, Rf);
+        }
+    }
+    return true;
+}
+
+template <typename T, bool kSample>
+__global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
+    constexpr int VEC = Elem<T>::kVec;
+    constexpr int CHUNK = chunk_elems<T>();
+    static_assert(CHUNK * sizeof(T) == kChunkBytes, "stats chunk must fill one ring stage");
+    static_assert(kResElems * 4 <= kResQOffset && kResQOffset + kResElems * 4 <= kChunkBytes, "residual stage");
+    static_assert(kResElems % kSegElems == 0 && kResElems / kSegElems == kCons, "one segment per consumer warp");
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (a.csr_ok && !__ldcg(a.csr_ok)) return;
+    const int nb = (a.n_chunks + kBlockChunks - 1) / kBlockChunks;  // stats blocks per row
+    const int total_blocks = a.rows * nb;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], kCons);
+        }
+        sm.abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    volatile int *abort_flag = &sm.abort;
+    const long long t_start = clock64();
+    auto timeout = [&]() {
+        *abort_flag = 1;
+        atomicOr(a.status, SV_FLAG_TIMEOUT);
+    };
+
+    if (warp == kProducer) {
+        if (lane == 0) {
+            int k = 0;  // ring stage counter
+            // next ring stage: wait until the consumers released it
+            auto claim = [&](int &s) -> bool {
+                s = k % kStages;
+                if (k >= kStages && !mbar_wait_bounded(&sm.empty[s], ((k / kStages) - 1) & 1, kWaitBudget)) {
+                    timeout();
+                    return false;
+                }
+                return !*abort_flag;
+            };
+            bool ok = true;
+            const uint32_t total_rb = kSample ? static_cast<uint32_t>(a.B) * static_cast<uint32_t>(a.n_rb) : 0u;
+            int jn = static_cast<int>(atomicAdd(a.sched + 0, 1u));
+            uint32_t pn = 0xffffffffu;  // next residual block claimed (one claim is kept in flight)
+            int cb = -1, crow = -1, cqrow = -1;  // the last decision read
+            float cM = 0.f, cinvS = 0.f;
+            while (ok) {
+                // 1. stats blocks first (row order, grid-wide counter): the decisions wait on them
+                if (jn < total_blocks) {
+                    const int j = jn;
+                    jn = static_cast<int>(atomicAdd(a.sched + 0, 1u));  // in flight while this block is issued
+                    const int row = j / nb;
+                    const int first = (j - row * nb) * kBlockChunks;
+                    const int cnt = min(kBlockChunks, a.n_chunks - first);
+                    for (int cc = 0; cc < cnt; ++cc) {
+                        int s;
+                        if (!claim(s)) {
+                            ok = false;
+                            break;
+                        }
+                        const int chunk = first + cc;
+                        const int c0 = chunk * CHUNK;
+                        const int n = min(CHUNK, a.V - c0);
+                        sm.tag[s] = Tag{kStats, row, chunk, n, 0, cc == cnt - 1 ? 1 : 0, 0.f, 0.f};
+                        const uint32_t bytes = static_cast<uint32_t>(n) * sizeof(T);
+                        mbar_arrive_expect_tx(&sm.full[s], bytes);
+                        bulk_g2s(sm.ring[s], reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(row) * a.V + c0,
+                                 bytes, &sm.full[s]);
+                        ++k;
+                    }
+                    continue;
+                }
+                if (!kSample) break;
+                // 2. residual blocks, claimed grid-wide in request-major order
+                if (pn == 0xffffffffu) pn = atomicAdd(a.sched + 2, 1u);
+                const uint32_t p = pn;
+                if (p >= total_rb) break;
+                pn = atomicAdd(a.sched + 2, 1u);  // the next claim, in flight meanwhile
+                const int b = static_cast<int>(p / static_cast<uint32_t>(a.n_rb));
+                const int blk = static_cast<int>(p % static_cast<uint32_t>(a.n_rb));
+                while (b != cb) {  // the request's decision
+                    const uint64_t w0 = ld_relaxed_u64(a.fdec + 2 * b);
+                    const uint64_t w1 = ld_relaxed_u64(a.fdec + 2 * b + 1);
+                    if ((w0 >> 32) != 0 && (w1 >> 32) != 0) {
+                        cb = b;
+                        crow = static_cast<int>(static_cast<uint32_t>(w1));
+                        cqrow = static_cast<int>(static_cast<uint32_t>(w1 >> 32)) - 2;
+                        cM = __uint_as_float(static_cast<uint32_t>(w0));
+                        cinvS = __uint_as_float(static_cast<uint32_t>(w0 >> 32) ^ 0x80000000u);
+                        break;
+                    }
+                    if (*abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    if (clock64() - t_start > kWaitBudget) {
+                        timeout();
+                        ok = false;
+                        break;
+                    }
+                    __nanosleep(kPollNs);
+                }
+                if (!ok) break;
+                if (crow < 0) continue;  // invalid request: nothing to draw
+                const bool has_q = cqrow >= 0;
+                for (int st = 0; st < kResBlockStages; ++st) {
+                    const int c0 = blk * kResBlockElems + st * kResElems;
+                    if (c0 >= a.V) break;
+                    const int n = min(kResElems, a.V - c0);
+                    int s;
+                    if (!claim(s)) {
+                        ok = false;
+                        break;
+                    }
+                    sm.tag[s] = Tag{kRes, b, c0 / kResElems, n, has_q ? 1 : 0, 0, cM, cinvS};
+                    const uint32_t zb = static_cast<uint32_t>(n) * sizeof(T);
+                    const uint32_t qb = has_q ? static_cast<uint32_t>(n) * 4u : 0u;
+                    mbar_arrive_expect_tx(&sm.full[s], zb + qb);
+                    bulk_g2s(sm.ring[s], reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(crow) * a.V + c0, zb,
+                             &sm.full[s]);
+                    if (has_q)
+                        bulk_g2s(sm.ring[s] + kResQOffset, a.q + static_cast<size_t>(cqrow) * a.V + c0, qb, &sm.full[s]);
+                    ++k;
+                }
+            }
+            // end of stream (a phase without data), or wait for issued copies on abort
+            int s;
+            if (ok && claim(s)) {
+                sm.tag[s] = Tag{kEnd, 0, 0, 0, 0, 0, 0.f, 0.f};
+                mbar_arrive(&sm.full[s]);
+            } else {
+                for (int kk = max(0, k - kStages); kk < k; ++kk)
+                    mbar_wait_bounded(&sm.full[kk % kStages], (kk / kStages) & 1, kWaitBudget);
+            }
+        }
+    } else if (warp == kWorker) {
+        for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
+            Sel sel;
+            if (!fused_decide<T, kSample>(a, b, lane, abort_flag, t_start, sel)) break;
+            if (!kSample) continue;
+            const float invS = 1.f / sel.S;
+            if (lane == 0) {
+                if (sel.valid) publish_decision(a.fdec + 2 * b, sel.M, invS, sel.row, sel.qrow);
+                else publish_decision(a.fdec + 2 * b, 0.f, 1.f, -1, -1);
+            }
+            if (sel.valid && !fused_draw<T>(a, b, sel, invS, lane, abort_flag, t_start)) break;
+        }
+    } else {
+        // consumers
+        int open = 0, seg_row = 0, seg_first = 0;
+        float ra;
+        int rb;
+        partial_identity<kSample>(ra, rb);
+        for (int k = 0;; ++k) {
+            const int s = k % kStages;
+            if (!mbar_wait_bounded(&sm.full[s], (k / kStages) & 1, kWaitBudget)) timeout();
+            if (*abort_flag) break;
+            const Tag tg = sm.tag[s];
+            if (tg.kind == kEnd) break;
+            if (tg.kind == kRes) {
+                float m = res_lane_sum<T>(sm.ring[s], warp, lane, tg.n, tg.has_q != 0, a.c, tg.M, tg.invS);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.empty[s]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
+                const int seg = tg.chunk * (kResElems / kSegElems) + warp;  // this warp's 256 tokens
+                if (lane == 0 && seg < a.n_seg)
+                    st_relaxed_u32(a.fmass + static_cast<size_t>(tg.row) * a.n_seg + seg, enc_mass(m));
+                continue;
+            }
+            if (!open) {  // first chunk of a stats block
+                open = 1;
+                seg_row = tg.row;
+                seg_first = tg.chunk;
+                partial_identity<kSample>(ra, rb);
+            }
+            const int c0 = tg.chunk * CHUNK;
+            const uint4 *stage = reinterpret_cast<const uint4 *>(sm.ring[s]);
+            float vals[kVecs][VEC];
+            int e0[kVecs];
+            if (tg.n == CHUNK) {
+#pragma unroll
+                for (int j = 0; j < kVecs; ++j) {
+                    const int v = warp * (kVecs * 32) + j * 32 + lane;
+                    e0[j] = v * VEC;
+                    unpack(stage[v], vals[j]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.empty[s]);
+                lane_accumulate<kSample, true, kVecs, VEC>(vals, e0, CHUNK, c0, a.c, ra, rb);
+            } else {
+#pragma unroll
+                for (int j = 0; j < kVecs; ++j) {
+                    const int v = warp * (kVecs * 32) + j * 32 + lane;
+                    e0[j] = v * VEC;
+                    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+                    if (e0[j] < tg.n) raw = stage[v];
+                    unpack(raw, vals[j]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.empty[s]);
+                lane_accumulate<kSample, false, kVecs, VEC>(vals, e0, tg.n, c0, a.c, ra, rb);
+            }
+            if (tg.last) {  // the block is complete: store this warp's partial of it
+                float wa = ra;
+                int wb = rb;
+                warp_partial_reduce<kSample>(wa, wb);
+                if (lane == 0)
+                    st_relaxed_u64(a.fpart + static_cast<size_t>(seg_row) * a.n_pe + (seg_first / kBlockChunks) * kCons +
+                                       warp,
+                                   enc_partial<kSample>(wa, wb));
+                open = 0;
+            }
+        }
+    }
+    // the last CTA out resets the counters (and, after a timeout, every record) for the next call
+    __shared__ int s_last;
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        const uint32_t done = atomicAdd(a.sched + 1, 1u);
+        s_last = (done + 1u == gridDim.x) ? 1 : 0;
+    }
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        if (kSample)
+            for (int i = tid; i < 2 * a.B; i += kThreads) a.fdec[i] = 0ull;
+        if (*reinterpret_cast<volatile uint32_t *>(a.status) & SV_FLAG_TIMEOUT) {
+            const size_t np = static_cast<size_t>(a.rows) * a.n_pe;
+            for (size_t i = tid; i < np; i += kThreads) a.fpart[i] = 0ull;
+            if (kSample) {
+                const size_t nm = static_cast<size_t>(a.B) * a.n_seg;
+                for (size_t i = tid; i < nm; i += kThreads) a.fmass[i] = 0u;
+            }
+        }
+        if (tid == 0) {
+            a.sched[0] = 0u;
+            a.sched[1] = 0u;
+            a.sched[2] = 0u;
+        }
+    }
+}
+
+}  // namespace fz
 
 // ---------------------------------------------------------------------------
 // Decide step over precomputed chunk partials (the fused LM-head path writes
@@ -986,17 +1650,22 @@ __global__ void __launch_bounds__(kThreads) csr_check_kernel(Args a, int *csr_ok
 // Host side
 // ---------------------------------------------------------------------------
 struct WsLayout {
-    size_t status, csr_ok, tickets1, dec, partials, tile_mass, total;
+    size_t status, csr_ok, tickets1, fpart, fmass, fdec, dec, partials, tile_mass, total;
+    bool rec_overflow;  // the fused records exceed the fixed region: they follow the rest, cleared per call
 };
 
 static inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Per-request counters live in a region of fixed capacity right after the
-// status words, whatever the call's shape, and every completed call leaves
-// the counters it used at zero.  A workspace therefore serves calls of any
-// shape once it has been zero-filled; only a call with more than kTicketCap
-// requests (whose counters reach into other regions) clears them first.
+// Per-request counters and the fused kernel's records live in a region of
+// fixed capacity right after the status words, whatever the call's shape,
+// and every completed call leaves what it used there at zero.  A workspace
+// therefore serves calls of any shape once it has been zero-filled; only a
+// call whose counters or records exceed the capacities clears them first.
 constexpr int kTicketCap = 16384;
+constexpr int kSchedWords = 8;
+constexpr size_t kRecPartCap = 32768;  // fused partial records (rows x n_pe)
+constexpr size_t kRecMassCap = 65536;  // fused segment masses (B x n_seg)
+constexpr size_t kRecDecCap = 8192;    // fused decision words (2 B)
 
 static WsLayout ws_layout(int B, int rows, int V, bool with_partials = true) {
     WsLayout L;
@@ -1005,10 +1674,25 @@ static WsLayout ws_layout(int B, int rows, int V, bool with_partials = true) {
     size_t o = 0;
     L.status = o; o = align256(o + 16);
     L.csr_ok = o; o = align256(o + 16);
-    L.tickets1 = o; o = align256(o + 4ull * static_cast<size_t>(B > kTicketCap ? B : kTicketCap));
+    const size_t cap = static_cast<size_t>(B > kTicketCap ? B : kTicketCap);
+    L.tickets1 = o; o = align256(o + 4ull * (cap + kSchedWords));  // tickets1 | sched
+    // fused records, sized for fp32 chunks (the larger count)
+    const size_t n_pe = ((n_chunks + fz::kBlockChunks - 1) / fz::kBlockChunks) * fz::kCons;
+    const size_t n_seg = (static_cast<size_t>(V) + kSegElems - 1) / kSegElems;
+    const size_t need_part = static_cast<size_t>(rows) * n_pe, need_mass = static_cast<size_t>(B) * n_seg,
+                 need_dec = 2ull * static_cast<size_t>(B);
+    L.rec_overflow = need_part > kRecPartCap || need_mass > kRecMassCap || need_dec > kRecDecCap;
+    L.fpart = o; o = align256(o + 8 * kRecPartCap);
+    L.fmass = o; o = align256(o + 4 * kRecMassCap);
+    L.fdec = o; o = align256(o + 8 * kRecDecCap);
     L.dec = o; o = align256(o + sizeof(Decision) * static_cast<size_t>(B));
     L.partials = o; o = align256(o + (with_partials ? sizeof(float2) * static_cast<size_t>(rows) * n_chunks : 0));
     L.tile_mass = o; o = align256(o + sizeof(float) * static_cast<size_t>(B) * n_tiles);
+    if (L.rec_overflow) {
+        L.fpart = o; o = align256(o + 8 * need_part);
+        L.fmass = o; o = align256(o + 4 * need_mass);
+        L.fdec = o; o = align256(o + 8 * need_dec);
+    }
     L.total = o;
     return L;
 }
@@ -1019,6 +1703,17 @@ void counter_region(int B, int rows, int V, size_t *offset, size_t *bytes) {
     const WsLayout L = ws_layout(B, rows, V);
     *offset = L.tickets1;
     *bytes = L.dec - L.tickets1;
+}
+
+// Counters and fused records of a workspace laid out as L.
+static void set_ws_records(Args &a, char *w, const WsLayout &L) {
+    a.tickets1 = reinterpret_cast<uint32_t *>(w + L.tickets1);
+    a.sched = a.tickets1 + (a.B > kTicketCap ? a.B : kTicketCap);
+    a.fpart = reinterpret_cast<uint64_t *>(w + L.fpart);
+    a.fmass = reinterpret_cast<uint32_t *>(w + L.fmass);
+    a.fdec = reinterpret_cast<uint64_t *>(w + L.fdec);
+    a.n_seg = (a.V + kSegElems - 1) / kSegElems;
+    a.n_rb = (a.V + kResBlockElems - 1) / kResBlockElems;
 }
 
 static void *g_prof_begin = nullptr;
@@ -1045,22 +1740,6 @@ int sm_count() {
         cached[dev] = n > 0 ? n : 1;
     }
     return cached[dev];
-}
-
-template <typename T, bool kSample>
-static void launch_tma_pass1(const Args &a, cudaStream_t s) {
-    static bool configured[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (!configured[dev]) {
-        cudaFuncSetAttribute(stats_tma_kernel<T, kSample>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(TmaSmem)));
-        configured[dev] = true;
-    }
-    const long long items = static_cast<long long>(a.rows) * a.n_chunks;
-    const unsigned grid = static_cast<unsigned>(items < sm_count() ? items : sm_count());
-    stats_tma_kernel<T, kSample><<<grid, kTmaThreads, sizeof(TmaSmem), s>>>(a);
 }
 
 template <typename T, bool kSample>
@@ -1095,27 +1774,51 @@ static void launch_pass2(const Args &a, cudaStream_t s) {
     cudaLaunchKernelEx(&cfg, residual_kernel<T, kVecPath>, a);
 }
 
+template <typename T, bool kSample>
+static void launch_fused(const Args &a, cudaStream_t s) {
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!configured[dev]) {
+        cudaFuncSetAttribute(fz::fused_kernel<T, kSample>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(fz::Smem)));
+        configured[dev] = true;
+    }
+    const int nb = (a.n_chunks + fz::kBlockChunks - 1) / fz::kBlockChunks;
+    const long long blocks = static_cast<long long>(a.rows) * nb;
+    const unsigned grid = static_cast<unsigned>(blocks < sm_count() ? blocks : sm_count());
+    fz::fused_kernel<T, kSample><<<grid, fz::kThreads, sizeof(fz::Smem), s>>>(a);
+}
+
 template <typename T>
 static sv_status run_typed(Args &a, bool sample, bool vec, cudaStream_t s) {
     a.n_chunks = (a.V + chunk_elems<T>() - 1) / chunk_elems<T>();
     int launches = 0;
+    a.n_pe = ((a.n_chunks + fz::kBlockChunks - 1) / fz::kBlockChunks) * fz::kCons;
     if (a.B > kTicketCap &&
-        cudaMemsetAsync(a.tickets1, 0, sizeof(uint32_t) * static_cast<size_t>(a.B), s) != cudaSuccess)
+        cudaMemsetAsync(a.tickets1, 0, sizeof(uint32_t) * (static_cast<size_t>(a.B) + kSchedWords), s) !=
+            cudaSuccess)
         return SV_ERR_CUDA;
     if (a.row_offsets) {
         csr_check_kernel<<<1, kThreads, 0, s>>>(a, const_cast<int *>(a.csr_ok));
         ++launches;
     }
     prof_begin(s);
-    if (sample) {
-        if (vec) launch_tma_pass1<T, true>(a, s); else launch_scalar_pass1<T, true>(a, s);
-    } else {
-        if (vec) launch_tma_pass1<T, false>(a, s); else launch_scalar_pass1<T, false>(a, s);
+    if (vec) {
+        // aligned rows: the whole step in one persistent kernel
+        if (sample) launch_fused<T, true>(a, s); else launch_fused<T, false>(a, s);
+        prof_end(s);
+        ++launches;
+        set_launches(launches);
+        return (cudaGetLastError() == cudaSuccess) ? SV_OK : SV_ERR_CUDA;
     }
+    if (sample) launch_scalar_pass1<T, true>(a, s);
+    else launch_scalar_pass1<T, false>(a, s);
     prof_end(s);
     ++launches;
     if (sample) {
-        if (vec) launch_pass2<T, true>(a, s); else launch_pass2<T, false>(a, s);
+        launch_pass2<T, false>(a, s);
         ++launches;
     }
     set_launches(launches);
@@ -1163,7 +1866,7 @@ static sv_status verify_common(const void *logits, sv_dtype dt, const float *q,
     a.c = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(temperature)) : 1.f;
     a.status = reinterpret_cast<uint32_t *>(w + L.status);
     a.csr_ok = row_offsets ? reinterpret_cast<const int *>(w + L.csr_ok) : nullptr;
-    a.tickets1 = reinterpret_cast<uint32_t *>(w + L.tickets1);
+    set_ws_records(a, w, L);
     a.dec = reinterpret_cast<Decision *>(w + L.dec);
     a.partials = reinterpret_cast<float2 *>(w + L.partials);
     a.tile_mass = reinterpret_cast<float *>(w + L.tile_mass);
@@ -1172,6 +1875,9 @@ static sv_status verify_common(const void *logits, sv_dtype dt, const float *q,
     const bool vec = aligned16(logits) && ((static_cast<size_t>(V) * esize) % 16 == 0) &&
                      (!q || (aligned16(q) && V % 4 == 0));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (vec && L.rec_overflow &&
+        cudaMemsetAsync(w + L.fpart, 0, L.total - L.fpart, s) != cudaSuccess)  // records beyond the fixed region
+        return SV_ERR_CUDA;
     if (dt == SV_F32) return run_typed<float>(a, sample, vec, s);
     return run_typed<__nv_bfloat16>(a, sample, vec, s);
 }
@@ -1224,7 +1930,7 @@ sv_status finish_from_partials(const float *logits, const float2 *partials, int 
     a.c = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(temperature)) : 1.f;
     a.status = reinterpret_cast<uint32_t *>(w + L.status);
     a.csr_ok = nullptr;
-    a.tickets1 = reinterpret_cast<uint32_t *>(w + L.tickets1);
+    set_ws_records(a, w, L);
     a.dec = reinterpret_cast<Decision *>(w + L.dec);
     a.partials = const_cast<float2 *>(partials);
     a.tile_mass = reinterpret_cast<float *>(w + L.tile_mass);
