@@ -213,6 +213,42 @@ def spec_profile_set_events(begin=None, end=None):
     _raise(load().spec_profile_set_events(b, e), "spec_profile_set_events")
 
 
+def bind_spec_verify_sample(logits, q, B, K, V, temperature, draft, uniforms, out_tokens, accept_len,
+                            ws, diag=None, stream=None):
+    """spec_verify_sample with its arguments checked and marshalled once: returns
+    a function of no arguments that makes the same C call again.  For loops that
+    issue the same call many times (the tensors must stay alive and in place)."""
+    _check(q, torch.float32, B * K * V, "q")
+    _check(draft, torch.int32, B * K, "draft")
+    _check(uniforms, torch.float32, B * (K + 1), "uniforms")
+    _check(out_tokens, torch.int32, B * (K + 1), "out_tokens")
+    _check(accept_len, torch.int32, B, "accept_len")
+    fn = load().spec_verify_sample
+    args = (_ptr(logits), _dtype_code(logits), _ptr(q), B, K, V, float(temperature), _ptr(draft),
+            _ptr(uniforms), _ptr(out_tokens), _ptr(accept_len), _ptr(diag), _ptr(ws), ws.numel(),
+            _stream(stream))
+
+    def call():
+        st = fn(*args)
+        if st != SV_OK:
+            raise SpecVerifyError(st, "spec_verify_sample")
+
+    return call
+
+
+def bind_spec_profile_set_events(begin=None, end=None):
+    """spec_profile_set_events with the event handles taken once (the events
+    must already have been recorded once, so that they exist)."""
+    fn = load().spec_profile_set_events
+    b = ctypes.c_void_p(begin.cuda_event) if begin is not None else None
+    e = ctypes.c_void_p(end.cuda_event) if end is not None else None
+
+    def call():
+        _raise(fn(b, e), "spec_profile_set_events")
+
+    return call
+
+
 def spec_last_launch_count() -> int:
     return int(load().spec_last_launch_count())
 

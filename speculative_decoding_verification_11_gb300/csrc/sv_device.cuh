@@ -14,7 +14,7 @@ constexpr int kTileElems = kThreads * 4;  // residual tile: 4 tokens per thread
 constexpr int kMaxRowsPerRequest = 256;   // SV_MAX_K + 1
 constexpr int kSegElems = 256;            // fused kernel: residual masses are kept per 256-token segment
 constexpr int kResStageElems = 4096;      // fused kernel: tokens of one residual ring stage
-constexpr int kResBlockStages = 1;        // fused kernel: stages per residual work block
+constexpr int kResBlockStages = 4;        // fused kernel: stages per residual work block
 constexpr int kResBlockElems = kResStageElems * kResBlockStages;
 
 // Elements per 16-byte vector and per stats chunk for each logits type.

@@ -1238,9 +1238,14 @@ __device__ bool fused_draw(const Args &a, int b, const Sel &sel, float invS, int
         __nanosleep(kPollNs);
     }
     DS sum{0.f, 0.f};
+    float clo[kRegSeg];  // in registers: mv[i], clo[i] become the lane's inclusive sums (double-single)
     if (in_regs) {
 #pragma unroll
-        for (int i = 0; i < kRegSeg; ++i) sum = ds_add_f(sum, mv[i]);
+        for (int i = 0; i < kRegSeg; ++i) {
+            sum = ds_add_f(sum, mv[i]);
+            mv[i] = sum.hi;
+            clo[i] = sum.lo;
+        }
     } else {
         for (int i = i0; i < i1; ++i) sum = ds_add_f(sum, dec_mass(ld_relaxed_u32(mw + i)));
     }
@@ -1257,14 +1262,17 @@ __device__ bool fused_draw(const Args &a, int b, const Sel &sel, float invS, int
     int found = -1;
     DS fb{0.f, 0.f};
     if (in_regs) {
+        // the first i whose inclusive sum passes t - P; compares independent of one another
+        const DS d = ds_add(t, DS{-P.hi, -P.lo});
+        DS prev{0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < kRegSeg; ++i) {
-            const DS Pn = ds_add_f(P, mv[i]);
-            if (found < 0 && i0 + i < i1 && ds_gt(Pn, t)) {
+            const DS ci{mv[i], clo[i]};
+            if (found < 0 && i0 + i < i1 && ds_gt(ci, d)) {
                 found = i0 + i;
-                fb = P;
+                fb = ds_add(P, prev);
             }
-            P = Pn;
+            prev = ci;
         }
     } else {
         for (int i = i0; i < i1; ++i) {
@@ -1410,7 +1418,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
             bool ok = true;
             const uint32_t total_rb = kSample ? static_cast<uint32_t>(a.B) * static_cast<uint32_t>(a.n_rb) : 0u;
             int jn = static_cast<int>(atomicAdd(a.sched + 0, 1u));
-            uint32_t pn = 0xffffffffu;  // next residual block claimed (one claim is kept in flight)
+            uint32_t pn = 0xffffffffu;     // next residual claim (in flight)
+            int nb_req = -1;               // request of the next claim whose decision words were read ahead
+            uint64_t nw0 = 0ull, nw1 = 0ull;
             int cb = -1, crow = -1, cqrow = -1;  // the last decision read
             float cM = 0.f, cinvS = 0.f;
             while (ok) {
@@ -1440,37 +1450,40 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                     continue;
                 }
                 if (!kSample) break;
-                // 2. residual blocks, claimed grid-wide in request-major order
+                // 2. residual blocks (kResBlockStages consecutive stages of one request's selected
+                // row), claimed grid-wide in request-major order.  One claim is kept in flight and
+                // its decision words are loaded while the current block's stages are issued.
                 if (pn == 0xffffffffu) pn = atomicAdd(a.sched + 2, 1u);
                 const uint32_t p = pn;
                 if (p >= total_rb) break;
-                pn = atomicAdd(a.sched + 2, 1u);  // the next claim, in flight meanwhile
                 const int b = static_cast<int>(p / static_cast<uint32_t>(a.n_rb));
                 const int blk = static_cast<int>(p % static_cast<uint32_t>(a.n_rb));
-                while (b != cb) {  // the request's decision
-                    const uint64_t w0 = ld_relaxed_u64(a.fdec + 2 * b);
-                    const uint64_t w1 = ld_relaxed_u64(a.fdec + 2 * b + 1);
-                    if ((w0 >> 32) != 0 && (w1 >> 32) != 0) {
-                        cb = b;
-                        crow = static_cast<int>(static_cast<uint32_t>(w1));
-                        cqrow = static_cast<int>(static_cast<uint32_t>(w1 >> 32)) - 2;
-                        cM = __uint_as_float(static_cast<uint32_t>(w0));
-                        cinvS = __uint_as_float(static_cast<uint32_t>(w0 >> 32) ^ 0x80000000u);
-                        break;
+                if (b != cb) {
+                    uint64_t w0 = (b == nb_req) ? nw0 : ld_relaxed_u64(a.fdec + 2 * b);
+                    uint64_t w1 = (b == nb_req) ? nw1 : ld_relaxed_u64(a.fdec + 2 * b + 1);
+                    while ((w0 >> 32) == 0 || (w1 >> 32) == 0) {  // not published yet
+                        if (*abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        if (clock64() - t_start > kWaitBudget) {
+                            timeout();
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(kPollNs);
+                        w0 = ld_relaxed_u64(a.fdec + 2 * b);
+                        w1 = ld_relaxed_u64(a.fdec + 2 * b + 1);
                     }
-                    if (*abort_flag) {
-                        ok = false;
-                        break;
-                    }
-                    if (clock64() - t_start > kWaitBudget) {
-                        timeout();
-                        ok = false;
-                        break;
-                    }
-                    __nanosleep(kPollNs);
+                    if (!ok) break;
+                    cb = b;
+                    crow = static_cast<int>(static_cast<uint32_t>(w1));
+                    cqrow = static_cast<int>(static_cast<uint32_t>(w1 >> 32)) - 2;
+                    cM = __uint_as_float(static_cast<uint32_t>(w0));
+                    cinvS = __uint_as_float(static_cast<uint32_t>(w0 >> 32) ^ 0x80000000u);
                 }
-                if (!ok) break;
-                if (crow < 0) continue;  // invalid request: nothing to draw
+                pn = atomicAdd(a.sched + 2, 1u);  // the next claim
+                if (crow < 0) continue;           // invalid request: nothing to draw
                 const bool has_q = cqrow >= 0;
                 for (int st = 0; st < kResBlockStages; ++st) {
                     const int c0 = blk * kResBlockElems + st * kResElems;
@@ -1490,6 +1503,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                     if (has_q)
                         bulk_g2s(sm.ring[s] + kResQOffset, a.q + static_cast<size_t>(cqrow) * a.V + c0, qb, &sm.full[s]);
                     ++k;
+                    if (st == 0 && pn < total_rb) {  // the next claim's decision, read ahead
+                        nb_req = static_cast<int>(pn / static_cast<uint32_t>(a.n_rb));
+                        if (nb_req != cb) {
+                            nw0 = ld_relaxed_u64(a.fdec + 2 * nb_req);
+                            nw1 = ld_relaxed_u64(a.fdec + 2 * nb_req + 1);
+                        } else {
+                            nb_req = -1;
+                        }
+                    }
                 }
             }
             // end of stream (a phase without data), or wait for issued copies on abort
