@@ -213,40 +213,44 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    for evs in ev:  # torch creates an event on its first record; the library re-records them
+    # Default: the K steps run back to back between one pair of events (the
+    # kernel is the whole step, launched with programmatic stream serialization,
+    # so nothing may sit between two launches).  With --l2-flush every step is
+    # bracketed by its own events, its flush outside them.
+    n_ev = args.steps if args.l2_flush else 1
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    for evs in ev:
         for e in evs:
             e.record(stream)
     torch.cuda.synchronize()
     clocks = Clocks(local)
-    launches = 0
+    # the same C call every step, marshalled once, so that the host stays ahead of the GPU
+    call = B_.bind_spec_verify_sample(logits, q, Bn, K, V, T, draft, uni, out, al, ws, stream=stream)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    # the same C call every step, marshalled once, so that the host stays ahead of the GPU
-    call = B_.bind_spec_verify_sample(logits, q, Bn, K, V, T, draft, uni, out, al, ws, stream=stream)
-    set_ev = [B_.bind_spec_profile_set_events(k0, k1) for _, _, k0, k1 in ev]
-    for i in range(args.steps):
-        if args.l2_flush:
+    if args.l2_flush:
+        for i in range(args.steps):
             flush.fill_(float(i))
-        s0, s1, _, _ = ev[i]
-        set_ev[i]()
-        s0.record(stream)
-        call()
-        s1.record(stream)
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+    else:
+        ev[0][0].record(stream)
+        for i in range(args.steps):
+            call()
+        ev[0][1].record(stream)
     launches = args.steps * B_.spec_last_launch_count()
-    B_.spec_profile_set_events(None, None)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
-    k_ms = [c.elapsed_time(d) for _, _, c, d in ev]
-    ms = statistics.mean(step_ms)
-    kms = statistics.mean(k_ms)
+    if args.l2_flush:
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    else:
+        ms = ev[0][0].elapsed_time(ev[0][1]) / args.steps
+    kms = ms * args.steps / launches  # one kernel per step: its mean duration, launch gap included
     if world > 1:
         t = torch.tensor([ms, kms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)

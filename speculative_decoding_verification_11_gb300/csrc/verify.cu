@@ -1384,7 +1384,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (a.csr_ok && !__ldcg(a.csr_ok)) return;
     const int nb = (a.n_chunks + kBlockChunks - 1) / kBlockChunks;  // stats blocks per row
     const int total_blocks = a.rows * nb;
     if (tid == 0) {
@@ -1396,6 +1395,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
         fence_mbar_init();
     }
     __syncthreads();
+    // Launched with programmatic stream serialization: the set-up above may
+    // overlap the previous kernel on the stream, whose results (the logits,
+    // this workspace) are visible only after this wait.
+    pdl_wait_prior_grid();
+    pdl_launch_dependents();
+    if (a.csr_ok && !__ldcg(a.csr_ok)) return;
     volatile int *abort_flag = &sm.abort;
     const long long t_start = clock64();
     auto timeout = [&]() {
@@ -1796,6 +1801,21 @@ static void launch_pass2(const Args &a, cudaStream_t s) {
     cudaLaunchKernelEx(&cfg, residual_kernel<T, kVecPath>, a);
 }
 
+template <typename KernelT>
+static cudaError_t launch_pdl(KernelT kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const Args &a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 template <typename T, bool kSample>
 static void launch_fused(const Args &a, cudaStream_t s) {
     static bool configured[64] = {false};
@@ -1810,7 +1830,7 @@ static void launch_fused(const Args &a, cudaStream_t s) {
     const int nb = (a.n_chunks + fz::kBlockChunks - 1) / fz::kBlockChunks;
     const long long blocks = static_cast<long long>(a.rows) * nb;
     const unsigned grid = static_cast<unsigned>(blocks < sm_count() ? blocks : sm_count());
-    fz::fused_kernel<T, kSample><<<grid, fz::kThreads, sizeof(fz::Smem), s>>>(a);
+    launch_pdl(fz::fused_kernel<T, kSample>, dim3(grid), dim3(fz::kThreads), sizeof(fz::Smem), s, a);
 }
 
 template <typename T>
@@ -1908,20 +1928,6 @@ static sv_status verify_common(const void *logits, sv_dtype dt, const float *q,
 // Workspace of finish_from_partials (the partials live elsewhere).
 size_t finish_workspace_size(int B, int rows, int V) { return ws_layout(B, rows, V, false).total; }
 
-template <typename KernelT>
-static cudaError_t launch_pdl(KernelT kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const Args &a) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, a);
-}
 
 // Decide + (sampling) residual draw over fp32 logits rows and per-(row, part)
 // partials that a previous kernel on `s` produced.  Launches 1 or 2 kernels.
