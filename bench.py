@@ -472,6 +472,139 @@ def run_lmhead(args):
     return 0
 
 
+def _alg_bytes(batch, al, n_rows_out):
+    """Algorithmic bytes of one verification call: every logit once, 16 B per
+    draft (z[x], q[x], x, u), the q row of every request that rejected (its
+    residual), and 4 B per output row and request."""
+    import torch
+    esize = 2 if batch.logits.dtype == torch.bfloat16 else 4
+    R, V = batch.rows, batch.V
+    nq = R - batch.B
+    k_i = (batch.row_offsets[1:] - batch.row_offsets[:-1] - 1).to(al.device)
+    rejected = int((al.to(torch.int64) <= k_i).sum()) if batch.q is not None else 0
+    return R * V * esize + nq * 16 + rejected * V * 4 + (n_rows_out + batch.B) * 4
+
+
+def run_config(args):
+    """The other workloads of the scope table, each a single JSON line:
+    greedy (B=32 K=5 V=32000 bf16), ragged (B=256, K_i ~ U{0..8}, V=151936),
+    tiny (B=1 K=4 V=1024: 1000 calls captured in one CUDA graph, and the same
+    1000 requests as one call)."""
+    import torch
+    from speculative_decoding_verification_11_gb300 import build, binding as B_, workloads as W
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    batch = {"greedy": W.greedy, "ragged": W.ragged, "tiny": W.tiny}[args.config]()
+    Bn, V, R = batch.B, batch.V, batch.rows
+    logits = batch.logits.to(dev)
+    draft = batch.draft.to(dev)
+    q = batch.q.to(dev) if batch.q is not None else None
+    uni = batch.uniforms.to(dev) if batch.uniforms is not None else None
+    offs = batch.row_offsets.to(dev)
+    out = torch.empty(R, dtype=torch.int32, device=dev)
+    al = torch.empty(Bn, dtype=torch.int32, device=dev)
+    ws = B_.workspace(B_.spec_verify_workspace_size(Bn, R, V), dev)
+    in_bytes = sum(t.numel() * t.element_size() for t in (logits, q) if t is not None)
+    small = in_bytes < 2 * (129 << 20)
+
+    def step():
+        if args.config == "greedy":
+            B_.spec_verify_greedy(logits, draft, Bn, batch.K, V, out, al, ws, stream=stream)
+        elif args.config == "ragged":
+            B_.spec_verify_ragged(logits, q, offs, Bn, R, V, batch.temperature, draft, uni, out, al, ws,
+                                  stream=stream)
+        else:
+            B_.spec_verify_sample(logits, q, Bn, batch.K, V, batch.temperature, draft, uni, out, al, ws,
+                                  stream=stream)
+
+    # inputs that fit in L2 are evicted before every timed call: a 256 MB write,
+    # then a 256 MB read so that no dirty line is left to be written back inside
+    # the timed call
+    fw = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if small else None
+    fr = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if small else None
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    n0 = B_.spec_last_launch_count()
+    clocks = Clocks(0)
+    clocks.start()
+    if small:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i in range(args.steps):
+            fw.fill_(float(i))
+            fr.sum()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        l2 = f"inputs {in_bytes / 1e6:.1f} MB < L2: 256 MB write then 256 MB read before every call, outside its events"
+    else:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        l2 = f"inputs {in_bytes / 1e6:.1f} MB > L2 (129 MB), no flush: calls back to back"
+    clk = clocks.stop()
+    alg = _alg_bytes(batch, al, R)
+    drafts = R - Bn
+    peak, peak_kind = _peaks()
+    achieved = alg / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "verified draft tokens/s", "value": drafts / (ms * 1e-3), "unit": "verified draft tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if logits.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+        "config": {"workload": f"{args.config} verify B={Bn} rows={R} V={V} T={batch.temperature}", "l2": l2},
+        "mean_accept_len": float(al.float().mean()),
+        "roofline": {"kernel": "fused_kernel (whole step)", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": alg, "ms_per_launch": ms},
+        "clocks": clk, "gpu_launches": args.steps * n0,
+    }
+    if args.config == "tiny":
+        # 1000 B=1 calls captured in one CUDA graph, replayed: latency per call
+        n_req = Bn
+        ws1 = B_.workspace(B_.spec_verify_workspace_size(1, 5, V), dev)
+        gs = torch.cuda.Stream(dev)
+        out1 = torch.empty(R, dtype=torch.int32, device=dev)
+        al1 = torch.empty(n_req, dtype=torch.int32, device=dev)
+        calls = [B_.bind_spec_verify_sample(logits[5 * i:5 * i + 5], q[4 * i:4 * i + 4], 1, 4, V,
+                                            batch.temperature, draft[4 * i:4 * i + 4], uni[5 * i:5 * i + 5],
+                                            out1[5 * i:5 * i + 5], al1[i:i + 1], ws1, stream=gs)
+                 for i in range(n_req)]
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            for c in calls[:3]:
+                c()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gs):
+            for c in calls:
+                c()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out1, out) and torch.equal(al1, al), "graph of B=1 calls differs from one B=1000 call"
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * n_req)
+        line["graph_b1"] = {"calls": n_req, "us_per_call": us, "verified_draft_tokens_per_s": 4 / (us * 1e-6),
+                            "note": "1000 B=1 calls in one CUDA graph, replayed 5 times; inputs stay in L2"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -482,13 +615,16 @@ def main():
     ap.add_argument("--l2-flush", action="store_true",
                     help="write a 256 MB buffer before every timed step (its dirty lines are written back "
                          "during the next step); by default the inputs, larger than L2, stand in for a flush")
-    ap.add_argument("--config", choices=["sampling", "lmhead"], default="sampling",
-                    help="sampling: the headline workload; lmhead: the fused LM-head front end")
+    ap.add_argument("--config", choices=["sampling", "lmhead", "greedy", "ragged", "tiny"], default="sampling",
+                    help="sampling: the headline workload; lmhead: the fused LM-head front end; "
+                         "greedy / ragged / tiny: the other verification workloads")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
     if args.config == "lmhead":
         return run_lmhead(args)
+    if args.config in ("greedy", "ragged", "tiny"):
+        return run_config(args)
     return run_ours(args)
 
 
