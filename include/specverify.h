@@ -212,6 +212,19 @@ sv_status spec_profile_set_events(void *begin, void *end);
 /* Number of kernels the last call on this thread launched (for accounting). */
 int spec_last_launch_count(void);
 
+/*
+ * Kernel choice for small vocabularies.  A call of spec_verify_greedy,
+ * spec_verify_sample, spec_verify_ragged or spec_verify_sample_noalloc whose
+ * requests each hold at most `bytes` of logits ((rows per request) x V x
+ * element size; for ragged calls the rows per request are bounded by
+ * min(256, rows - B + 1)) runs one CTA per request with the request's rows in
+ * shared memory; larger requests stream through one persistent kernel.  Both
+ * compute the same step.  0 sends every call to the streaming kernel.
+ * Default 49152.  Process-wide (an atomic); returns the previous value.  The
+ * pages have no counterpart to it: it is a tuning knob of this library.
+ */
+size_t spec_set_small_kernel_limit(size_t bytes);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,7 @@ EXPORTS = (
     "spec_verify_workspace_size", "spec_verify_greedy", "spec_verify_sample", "spec_verify_ragged",
     "spec_lmhead_workspace_size", "spec_lmhead_verify", "spec_verify_last_device_status",
     "spec_status_string", "spec_profile_set_events", "spec_last_launch_count",
-    "spec_verify_sample_noalloc",
+    "spec_verify_sample_noalloc", "spec_set_small_kernel_limit",
 )
 
 _lock = threading.Lock()
@@ -64,6 +64,7 @@ def load() -> ctypes.CDLL:
             "spec_profile_set_events": (I, [P, P]),
             "spec_last_launch_count": (I, []),
             "spec_verify_sample_noalloc": (I, [P, I, P, I, I, I, F, P, P, P, P, P, P]),
+            "spec_set_small_kernel_limit": (Z, [Z]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -247,6 +248,13 @@ def bind_spec_profile_set_events(begin=None, end=None):
         _raise(fn(b, e), "spec_profile_set_events")
 
     return call
+
+
+def spec_set_small_kernel_limit(nbytes: int) -> int:
+    """Largest per-request logits footprint (bytes) that runs on the
+    request-per-CTA kernel; 0 sends every call to the streaming kernel.
+    Returns the previous value."""
+    return int(load().spec_set_small_kernel_limit(int(nbytes)))
 
 
 def spec_last_launch_count() -> int:

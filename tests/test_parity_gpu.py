@@ -45,6 +45,17 @@ def _gpu_ragged(batch, dev, T=None, diag=True):
     return out.cpu().numpy(), al.cpu().numpy(), (dg.cpu().numpy() if dg is not None else None)
 
 
+@pytest.fixture(params=["small", "stream"])
+def kernel(request, cuda_device):
+    """Runs a test on each kernel: "small" raises the request-per-CTA kernel's
+    limit to 192 KB of logits per request (so that every shape that fits its
+    shared memory takes it), "stream" sends every call to the persistent
+    streaming kernel."""
+    prev = B_.spec_set_small_kernel_limit(192 * 1024 if request.param == "small" else 0)
+    yield request.param
+    B_.spec_set_small_kernel_limit(prev)
+
+
 def _status(dev):
     ws = api._default_ws[(str(dev), torch.cuda.current_stream(dev).cuda_stream)].buf
     return B_.spec_verify_last_device_status(ws)
@@ -135,10 +146,10 @@ GREEDY_SHAPES = [(1, 3), (7, 2), (1000, 5), (8191, 1), (8192, 4), (16385, 3), (4
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("V,K", GREEDY_SHAPES)
-def test_greedy_shapes_with_ties(cuda_device, dtype, V, K):
+def test_greedy_shapes_with_ties(cuda_device, kernel, dtype, V, K):
     b = _rand_batch(10 + V + K, B=9, K=K, V=V, dtype=dtype, T=0.0, ties=True)
     out, al, _ = _gpu_fixed(b, cuda_device)
-    compare_greedy(f"greedy V={V} K={K} {dtype}", b.row_offsets, out, al, _oracle(b))
+    compare_greedy(f"greedy V={V} K={K} {dtype} {kernel}", b.row_offsets, out, al, _oracle(b))
 
 
 SAMPLE_SHAPES = [(5, 2, 1.0), (1000, 4, 0.7), (4097, 3, 1.3), (8192, 4, 1.0), (10007, 5, 0.9),
@@ -147,20 +158,20 @@ SAMPLE_SHAPES = [(5, 2, 1.0), (1000, 4, 0.7), (4097, 3, 1.3), (8192, 4, 1.0), (1
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("V,K,T", SAMPLE_SHAPES)
-def test_sampling_shapes(cuda_device, dtype, V, K, T):
+def test_sampling_shapes(cuda_device, kernel, dtype, V, K, T):
     b = _rand_batch(100 + V + K, B=24, K=K, V=V, dtype=dtype, T=T)
     out, al, dg = _gpu_fixed(b, cuda_device)
-    compare_sampling(f"sample V={V} K={K} T={T} {dtype}", b.row_offsets, out, al, dg, _oracle(b))
+    compare_sampling(f"sample V={V} K={K} T={T} {dtype} {kernel}", b.row_offsets, out, al, dg, _oracle(b))
 
 
-def test_sampling_k_zero_is_bonus_only(cuda_device):
+def test_sampling_k_zero_is_bonus_only(cuda_device, kernel):
     b = _rand_batch(5, B=40, K=0, V=3000, dtype=torch.float32, T=1.0)
     out, al, dg = _gpu_fixed(b, cuda_device)
     assert np.all(al == 1)
     compare_sampling("sample K=0", b.row_offsets, out, al, dg, _oracle(b))
 
 
-def test_ragged_small_mixed(cuda_device):
+def test_ragged_small_mixed(cuda_device, kernel):
     g = torch.Generator().manual_seed(77)
     ks = [0, 3, 0, 8, 1, 255, 2]
     b = W.make_sampling_batch("r", 77, B=len(ks), K=None, V=3001, T=0.8, logit_sigma=2.0,
@@ -169,10 +180,21 @@ def test_ragged_small_mixed(cuda_device):
     compare_sampling("ragged small incl. K=255", b.row_offsets, out, al, dg, _oracle(b))
 
 
+def test_ragged_small_vocab_long_requests(cuda_device, kernel):
+    """V = 40: even a request of 256 rows fits the request-per-CTA kernel."""
+    ks = [0, 3, 255, 17, 1, 64, 0]
+    b = W.make_sampling_batch("rs", 91, B=len(ks), K=None, V=40, T=1.1, logit_sigma=1.5,
+                              noise_sigma=0.6, k_list=ks)
+    out, al, dg = _gpu_ragged(b, cuda_device)
+    compare_sampling(f"ragged V=40 incl. K=255 {kernel}", b.row_offsets, out, al, dg, _oracle(b))
+    out, al, _ = _gpu_ragged(b, cuda_device, T=0.0)
+    compare_greedy(f"ragged greedy V=40 incl. K=255 {kernel}", b.row_offsets, out, al, _oracle(b, temperature=0.0))
+
+
 # --------------------------------------------------------------------------
 # special cases and errors
 # --------------------------------------------------------------------------
-def test_q_equals_p_accepts_everything(cuda_device):
+def test_q_equals_p_accepts_everything(cuda_device, kernel):
     B, K, V, T = 64, 4, 5000, 0.9
     g = torch.Generator().manual_seed(8)
     z = torch.randn(B * (K + 1), V, generator=g) * 2
@@ -189,7 +211,7 @@ def test_q_equals_p_accepts_everything(cuda_device):
     compare_sampling("q == p", b.row_offsets, out, al, dg, orc)
 
 
-def test_invalid_draft_id_is_isolated(cuda_device):
+def test_invalid_draft_id_is_isolated(cuda_device, kernel):
     b = _rand_batch(3, B=6, K=3, V=2000, dtype=torch.float32, T=1.0)
     x = b.draft.clone()
     x[5] = 2000  # request 1, position 2
@@ -207,7 +229,7 @@ def test_invalid_draft_id_is_isolated(cuda_device):
     assert _status(cuda_device) == (B_.SV_OK, 0)
 
 
-def test_malformed_offsets_invalidate_call(cuda_device):
+def test_malformed_offsets_invalidate_call(cuda_device, kernel):
     dev = cuda_device
     V = 500
     z = torch.randn(10, V, device=dev)
@@ -228,7 +250,7 @@ def test_malformed_offsets_invalidate_call(cuda_device):
     assert torch.all(al >= 1)
 
 
-def test_zero_residual_falls_back_to_p(cuda_device):
+def test_zero_residual_falls_back_to_p(cuda_device, kernel):
     dev = cuda_device
     z = torch.log(torch.tensor([[0.5, 0.5], [0.5, 0.5]])).to(dev)
     q = torch.tensor([[0.6, 0.6]], device=dev)
@@ -248,7 +270,7 @@ def test_empty_batch(cuda_device):
     assert out.numel() == 0 and al.numel() == 0
 
 
-def test_repeat_calls_identical_and_canaries(cuda_device):
+def test_repeat_calls_identical_and_canaries(cuda_device, kernel):
     dev = cuda_device
     b = _rand_batch(21, B=16, K=4, V=9000, dtype=torch.float32, T=1.0)
     logits, q, x, u = b.logits.to(dev), b.q.to(dev), b.draft.to(dev), b.uniforms.to(dev)
@@ -278,7 +300,7 @@ def test_repeat_calls_identical_and_canaries(cuda_device):
 # the emitted token's law on the GPU (10^6 trials, V = 16)
 # --------------------------------------------------------------------------
 @pytest.mark.parametrize("variant", ["near", "onehot", "zeros", "far"])
-def test_emitted_token_law_chisquare_gpu(cuda_device, variant):
+def test_emitted_token_law_chisquare_gpu(cuda_device, kernel, variant):
     from test_oracle_pins import _chisq_pvalue, _q_variants
     rng = np.random.default_rng(321)
     V, K, T, n = 16, 2, 1.0, 1_000_000
@@ -299,7 +321,7 @@ def test_emitted_token_law_chisquare_gpu(cuda_device, variant):
         sel = al > j
         counts = np.bincount(out[sel, j], minlength=V).astype(np.float64)
         pv.append(_chisq_pvalue(counts, p[j]))
-    record(f"chi-square GPU {variant}", {"pvalues": pv, "trials": n, "mean_al": float(al.mean())})
+    record(f"chi-square GPU {variant} {kernel}", {"pvalues": pv, "trials": n, "mean_al": float(al.mean())})
     assert min(pv) > 1e-3
 
 
