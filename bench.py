@@ -605,6 +605,92 @@ def run_config(args):
     return 0
 
 
+def run_kv(args):
+    """KV-cache bookkeeping after verification: spec_kv_reserve then
+    spec_kv_rollback with every draft rejected (accept length 1: the most
+    blocks returned), which leaves the cache as it was, so steps repeat on the
+    same state.  K = 4 drafts per request, 16-token blocks, lengths up to 4096."""
+    import numpy as np
+    import torch
+    from speculative_decoding_verification_11_gb300 import build, binding as B_
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for Bn in (64, 4096):
+        rng = np.random.default_rng(7 + Bn)
+        bs, K, max_blocks = 16, 4, 264
+        seq = rng.integers(1, 4096, size=Bn).astype(np.int32)
+        n_ids = Bn * max_blocks
+        ids = rng.permutation(n_ids).astype(np.int32)
+        bt = np.full((Bn, max_blocks), -1, dtype=np.int32)
+        k = 0
+        for b in range(Bn):
+            nb = -(-int(seq[b]) // bs)
+            bt[b, :nb] = ids[k:k + nb]
+            k += nb
+        free = np.full(n_ids, -1, dtype=np.int32)
+        free[:n_ids - k] = ids[k:]
+        g_bt = torch.from_numpy(bt).to(dev)
+        g_seq = torch.from_numpy(seq).to(dev)
+        g_free = torch.from_numpy(free).to(dev)
+        g_fc = torch.tensor([n_ids - k], dtype=torch.int32, device=dev)
+        g_K = torch.full((Bn,), K, dtype=torch.int32, device=dev)
+        g_al = torch.ones(Bn, dtype=torch.int32, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def step():
+            B_.spec_kv_reserve(g_bt, g_seq, g_free, g_fc, g_K, bs, st, stream=stream)
+            B_.spec_kv_rollback(g_bt, g_seq, g_free, g_fc, g_K, g_al, bs, st, stream=stream)
+
+        for _ in range(max(args.warmup, 3)):
+            step()
+        torch.cuda.synchronize()
+        # launch-bound: the K steps are captured in one CUDA graph
+        g = torch.cuda.CUDAGraph()
+        gs = torch.cuda.Stream(dev)
+        gs.wait_stream(stream)
+        with torch.cuda.graph(g, stream=gs):
+            for _ in range(args.steps):
+                B_.spec_kv_reserve(g_bt, g_seq, g_free, g_fc, g_K, bs, st, stream=gs)
+                B_.spec_kv_rollback(g_bt, g_seq, g_free, g_fc, g_K, g_al, bs, st, stream=gs)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        assert st.item() == 0 and np.array_equal(g_bt.cpu().numpy(), bt), "state must return to itself"
+        new_blocks = sum(-(-(int(s) + K) // bs) - (-(-int(s) // bs)) for s in seq)
+        # bytes: lengths and counts read twice, accept lengths, touched table entries
+        # (checked, then written), free-list slots (read, then written)
+        alg = Bn * 4 * 5 + new_blocks * 4 * 6
+        res[f"B={Bn}"] = {"us_per_step": ms * 1e3, "blocks_moved_per_step": 2 * new_blocks,
+                          "algorithmic_bytes": alg, "achieved_gbs": alg / (ms * 1e-3) / 1e9}
+    peak, peak_kind = _peaks()
+    head = res["B=64"]
+    line = {
+        "metric": "KV bookkeeping steps/s (reserve + rollback)", "value": 1e6 / head["us_per_step"],
+        "unit": "steps/s", "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": head["us_per_step"] * 1e-3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": {"workload": "paged KV reserve + rollback, B=64 and 4096, K=4, 16-token blocks, "
+                               "every draft rejected", "l2": "state stays in L2 (launch-bound, one CTA)"},
+        "roofline": {"kernel": "kvb::reserve_kernel + kvb::rollback_kernel", "bound": "hbm",
+                     "achieved": head["achieved_gbs"], "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": head["achieved_gbs"] / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": head["algorithmic_bytes"] / 2,
+                     "ms_per_launch": head["us_per_step"] * 1e-3 / 2,
+                     "note": "latency-bound: one CTA and two dependent launches per step"},
+        "batches": res, "gpu_launches": 2 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -615,7 +701,7 @@ def main():
     ap.add_argument("--l2-flush", action="store_true",
                     help="write a 256 MB buffer before every timed step (its dirty lines are written back "
                          "during the next step); by default the inputs, larger than L2, stand in for a flush")
-    ap.add_argument("--config", choices=["sampling", "lmhead", "greedy", "ragged", "tiny"], default="sampling",
+    ap.add_argument("--config", choices=["sampling", "lmhead", "greedy", "ragged", "tiny", "kv"], default="sampling",
                     help="sampling: the headline workload; lmhead: the fused LM-head front end; "
                          "greedy / ragged / tiny: the other verification workloads")
     args = ap.parse_args()
@@ -625,6 +711,8 @@ def main():
         return run_lmhead(args)
     if args.config in ("greedy", "ragged", "tiny"):
         return run_config(args)
+    if args.config == "kv":
+        return run_kv(args)
     return run_ours(args)
 
 

@@ -89,6 +89,8 @@ typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 #define SV_FLAG_BAD_OFFSETS 0x2u    /* CSR offsets not increasing, or K_b > SV_MAX_K */
 #define SV_FLAG_ZERO_RESIDUAL 0x4u  /* informational: a draw fell back to p */
 #define SV_FLAG_TIMEOUT 0x8u        /* a bounded wait expired */
+#define SV_FLAG_KV_OUT_OF_BLOCKS 0x10u  /* spec_kv_reserve: the free list is short */
+#define SV_FLAG_KV_BAD_INPUT 0x20u      /* spec_kv_reserve / _rollback: an input breaks a rule */
 
 /* Largest number of drafted tokens per request. */
 #define SV_MAX_K 255
@@ -224,6 +226,61 @@ int spec_last_launch_count(void);
  * pages have no counterpart to it: it is a tuning knob of this library.
  */
 size_t spec_set_small_kernel_limit(size_t bytes);
+
+/*
+ * Paged KV-cache bookkeeping around verification ("Speculative Decoding in
+ * Large Language Models", section 4, "Segmented Block Allocation
+ * (PagedAttention)": fixed-size blocks, block pointers for the speculative
+ * tokens, rejected positions return their pointers to the global free list
+ * with no copy; "Speculative Decoding in Production: Accelerating LLM
+ * Inference via Custom Draft Models", "Serving Architecture and KV Cache
+ * Syncing": with M of K drafts accepted, K - M slots are evicted, in the
+ * draft's cache and in the target's; call once per cache).
+ *
+ * A cache is, in device memory owned by the caller:
+ *   block_table  int32 [B x max_blocks], row b = physical block ids of
+ *                request b's logical blocks, -1 = no block;
+ *   seq_len      int32 [B], tokens of request b with valid KV;
+ *   free_ids     int32 [capacity], a stack of free block ids;
+ *   free_count   int32 [1], entries of free_ids in use (its top).
+ * Logical block i of a request holds positions [i bs, (i + 1) bs).
+ * Both calls are one kernel on `stream`, stream-ordered and asynchronous,
+ * touch block ids only (no KV data), and are deterministic.  A call whose
+ * inputs break a rule changes nothing and ORs a flag into *status (a device
+ * uint32 owned by the caller, zero until a flag is set); argument errors are
+ * returned before any launch.
+ */
+
+/*
+ * Blocks for the speculative slots: request b's table is extended to cover
+ * positions [0, seq_len[b] + n_new[b]) (seq_len is not changed).  Blocks are
+ * popped from the top of the stack; request 0 takes the lowest stack slots of
+ * the popped range, each request its blocks in logical order.  If the stack
+ * holds fewer blocks than the batch needs, nothing changes and
+ * SV_FLAG_KV_OUT_OF_BLOCKS is set.  Rules: n_new >= 0, seq_len >= 0, the new
+ * length fits the table, and the entries to fill hold no block (else
+ * SV_FLAG_KV_BAD_INPUT).
+ */
+sv_status spec_kv_reserve(int32_t *block_table, const int32_t *seq_len, const int32_t *free_ids,
+                          int32_t *free_count, const int32_t *n_new, int B, int max_blocks,
+                          int block_size, uint32_t *status, void *stream);
+
+/*
+ * After verification: request b wrote n_spec[b] speculative slots after its
+ * seq_len[b] valid ones; accept_len[b] (from a verification call: AL, or 0
+ * for an invalid request) - 1 accepted drafts keep their KV, the final emitted
+ * token gets its KV in the next step.  seq_len[b] += max(accept_len[b] - 1,
+ * 0); the blocks wholly beyond the new length (logical blocks
+ * ceil(new_len / bs) .. ceil((seq_len + n_spec) / bs) - 1) are pushed on the
+ * stack in request order, each request's in logical order, and their table
+ * entries set to -1.  Rules: counts >= 0, accept_len <= n_spec + 1, the
+ * span fits the table, every entry to free holds a block, and the stack does
+ * not overflow `capacity` (else SV_FLAG_KV_BAD_INPUT).
+ */
+sv_status spec_kv_rollback(int32_t *block_table, int32_t *seq_len, int32_t *free_ids,
+                           int32_t *free_count, const int32_t *n_spec, const int32_t *accept_len,
+                           int B, int max_blocks, int block_size, int capacity, uint32_t *status,
+                           void *stream);
 
 #ifdef __cplusplus
 }

@@ -18,13 +18,14 @@ from . import build as _build
 SV_OK, SV_ERR_INVALID, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, SV_ERR_TIMEOUT, SV_ERR_WORKSPACE = range(6)
 SV_F32, SV_BF16 = 0, 1
 SV_FLAG_BAD_TOKEN, SV_FLAG_BAD_OFFSETS, SV_FLAG_ZERO_RESIDUAL, SV_FLAG_TIMEOUT = 1, 2, 4, 8
+SV_FLAG_KV_OUT_OF_BLOCKS, SV_FLAG_KV_BAD_INPUT = 0x10, 0x20
 SV_MAX_K = 255
 
 EXPORTS = (
     "spec_verify_workspace_size", "spec_verify_greedy", "spec_verify_sample", "spec_verify_ragged",
     "spec_lmhead_workspace_size", "spec_lmhead_verify", "spec_verify_last_device_status",
     "spec_status_string", "spec_profile_set_events", "spec_last_launch_count",
-    "spec_verify_sample_noalloc", "spec_set_small_kernel_limit",
+    "spec_verify_sample_noalloc", "spec_set_small_kernel_limit", "spec_kv_reserve", "spec_kv_rollback",
 )
 
 _lock = threading.Lock()
@@ -65,6 +66,8 @@ def load() -> ctypes.CDLL:
             "spec_last_launch_count": (I, []),
             "spec_verify_sample_noalloc": (I, [P, I, P, I, I, I, F, P, P, P, P, P, P]),
             "spec_set_small_kernel_limit": (Z, [Z]),
+            "spec_kv_reserve": (I, [P, P, P, P, P, I, I, I, P, P]),
+            "spec_kv_rollback": (I, [P, P, P, P, P, P, I, I, I, I, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -255,6 +258,38 @@ def spec_set_small_kernel_limit(nbytes: int) -> int:
     request-per-CTA kernel; 0 sends every call to the streaming kernel.
     Returns the previous value."""
     return int(load().spec_set_small_kernel_limit(int(nbytes)))
+
+
+def _check_kv(block_table, seq_len, free_ids, free_count, status):
+    _check(block_table, torch.int32, None, "block_table")
+    _check(seq_len, torch.int32, block_table.shape[0], "seq_len")
+    _check(free_ids, torch.int32, None, "free_ids")
+    _check(free_count, torch.int32, 1, "free_count")
+    if status is None or status.dtype not in (torch.int32, torch.uint32) or status.numel() < 1:
+        raise TypeError("status: a device int32/uint32 word is required")
+    if block_table.dim() != 2:
+        raise ValueError("block_table: expected (B, max_blocks)")
+
+
+def spec_kv_reserve(block_table, seq_len, free_ids, free_count, n_new, block_size, status, stream=None):
+    _check_kv(block_table, seq_len, free_ids, free_count, status)
+    B, max_blocks = block_table.shape
+    _check(n_new, torch.int32, B, "n_new")
+    st = load().spec_kv_reserve(_ptr(block_table), _ptr(seq_len), _ptr(free_ids), _ptr(free_count), _ptr(n_new),
+                                B, max_blocks, int(block_size), _ptr(status), _stream(stream))
+    _raise(st, "spec_kv_reserve")
+
+
+def spec_kv_rollback(block_table, seq_len, free_ids, free_count, n_spec, accept_len, block_size, status,
+                     stream=None):
+    _check_kv(block_table, seq_len, free_ids, free_count, status)
+    B, max_blocks = block_table.shape
+    _check(n_spec, torch.int32, B, "n_spec")
+    _check(accept_len, torch.int32, B, "accept_len")
+    st = load().spec_kv_rollback(_ptr(block_table), _ptr(seq_len), _ptr(free_ids), _ptr(free_count), _ptr(n_spec),
+                                 _ptr(accept_len), B, max_blocks, int(block_size), free_ids.numel(), _ptr(status),
+                                 _stream(stream))
+    _raise(st, "spec_kv_rollback")
 
 
 def spec_last_launch_count() -> int:

@@ -105,3 +105,20 @@ def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "lib_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         binding.load()
+
+
+def test_kv_argument_errors_return_before_launch(lib):
+    """Argument errors of the KV-cache calls come back synchronously, with no
+    launch (the pointers are never touched)."""
+    P = ctypes.c_void_p(0x1000)
+    ok_args = dict(B=4, max_blocks=8, bs=16)
+    assert lib.spec_kv_reserve(P, P, P, P, P, 4, 0, 16, P, None) == binding.SV_ERR_INVALID   # max_blocks
+    assert lib.spec_kv_reserve(P, P, P, P, P, 4, 8, 0, P, None) == binding.SV_ERR_INVALID    # block size
+    assert lib.spec_kv_reserve(P, None, P, P, P, 4, 8, 16, P, None) == binding.SV_ERR_INVALID
+    assert lib.spec_kv_reserve(P, P, P, P, P, -1, 8, 16, P, None) == binding.SV_ERR_INVALID
+    assert lib.spec_kv_reserve(None, None, None, None, None, 0, 8, 16, None, None) == binding.SV_OK  # empty
+    assert lib.spec_kv_rollback(P, P, P, P, P, P, 4, 8, 16, -1, P, None) == binding.SV_ERR_INVALID  # capacity
+    assert lib.spec_kv_rollback(P, P, P, P, P, None, 4, 8, 16, 10, P, None) == binding.SV_ERR_INVALID
+    assert lib.spec_kv_rollback(P, P, P, P, P, P, 4, 8, 16, 10, None, None) == binding.SV_ERR_INVALID
+    assert lib.spec_kv_rollback(None, None, None, None, None, None, 0, 8, 16, 0, None, None) == binding.SV_OK
+    del ok_args
