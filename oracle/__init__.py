@@ -14,6 +14,12 @@ Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``
   softmax_rows             pinned: closed forms.
   lmhead_logits            pinned: direct sum on small shapes.
   speedup.*                pinned: the worked numbers printed on the pages.
+  kv_blocks.*              pinned: token-by-token simulation, conservation of
+                           block ids, reserve + full rejection = identity,
+                           K - M evictions (tests/test_oracle_pins_kv.py).
+  draft.*                  pinned: Philox4x32-10 known-answer vectors, exact
+                           rational enumeration of the draw, chi-square of the
+                           draws (tests/test_oracle_pins_draft.py).
 """
 from __future__ import annotations
 

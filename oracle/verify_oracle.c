@@ -264,3 +264,81 @@ int oracle_verify_batch(const void *logits, int zdtype, const float *q,
     free(work);
     return bad;
 }
+
+/* ------------------------------------------------------------------------
+ * Draft-side sampling (the step before verification: q and x for the drafted
+ * positions; the proof of "Speculative Decoding in Large Language Models",
+ * section 2, assumes x ~ q).  The uniforms are drawn, not passed in, so this
+ * side has its own counter-based generator, written from its published
+ * definition: Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random
+ * numbers: as easy as 1, 2, 3", SC 2011): ten rounds of two 32x32 -> 64-bit
+ * products with multipliers 0xD2511F53 and 0xCD9E8D57, the key bumped by the
+ * Weyl constants 0x9E3779B9 and 0xBB67AE85 between rounds.
+ * ---------------------------------------------------------------------- */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        uint32_t n0 = hi1 ^ c1 ^ k0;
+        uint32_t n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+/*
+ * The uniform of draw `index` of stream `stream` under `seed` (the reading
+ * used on both sides): counter (index low word, stream, index high word, 0),
+ * key (seed low word, seed high word); u = ((w0 >> 9) + 1/2) 2^-23, in (0, 1).
+ */
+double oracle_philox_uniform(uint64_t seed, uint64_t index, uint32_t stream)
+{
+    uint32_t ctr[4] = {(uint32_t)index, stream, (uint32_t)(index >> 32), 0u};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    oracle_philox4x32_10(ctr, key, out);
+    return ((double)(out[0] >> 9) + 0.5) * 0x1p-23;
+}
+
+/*
+ * Inverse CDF in ascending index over weights r >= 0: the smallest v with
+ * C(v) > u R (R = sum of r); if rounding leaves none, the largest v with
+ * r(v) > 0.  *near_tie = 1 when a boundary C(v)/R lies within `band` of u.
+ */
+int64_t oracle_draw_inverse_cdf(const double *r, int64_t V, double u, double band, int *near_tie)
+{
+    double R = 0.0;
+    for (int64_t v = 0; v < V; ++v)
+        R += r[v];
+    double t = u * R, C = 0.0, Cprev = 0.0;
+    *near_tie = 0;
+    for (int64_t v = 0; v < V; ++v) {
+        Cprev = C;
+        C += r[v];
+        if (C > t) {
+            if (u - Cprev / R < band || C / R - u < band)
+                *near_tie = 1;
+            return v;
+        }
+    }
+    *near_tie = 1;
+    for (int64_t v = V - 1; v >= 0; --v)
+        if (r[v] > 0.0)
+            return v;
+    return -1;
+}
