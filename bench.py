@@ -691,6 +691,72 @@ def run_kv(args):
     return 0
 
 
+def run_draft(args):
+    """Draft head + draft sampling at the fused workload's draft head: M = 128
+    rows (16 requests x 8 positions), d = 2048, V = 128256, T = 1: the tcgen05
+    GEMM writes fp32 logits into q's buffer, then one CTA per row turns them
+    into q and draws x with Philox."""
+    import torch
+    from speculative_decoding_verification_11_gb300 import build, binding as B_
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    M, d, V, T = 128, 2048, 128256, 1.0
+    g = torch.Generator().manual_seed(1005)
+    h = torch.randn(M, d, generator=g).to(torch.bfloat16).to(dev)
+    w = (torch.randn(V, d, generator=g) * 0.02).to(torch.bfloat16).to(dev)
+    q = torch.empty(M, V, device=dev)
+    x = torch.empty(M, dtype=torch.int32, device=dev)
+    ws = B_.workspace(B_.spec_draft_workspace_size(M, d, V), dev)
+    for i in range(max(args.warmup, 3)):
+        B_.spec_draft_sample(h, w, T, 1005, i * M, q, x, ws, stream=stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e4 in ev:
+        for e in e4:
+            e.record(stream)
+    torch.cuda.synchronize()
+    clocks = Clocks(0)
+    clocks.start()
+    for i in range(args.steps):
+        s0, s1, k0, k1 = ev[i]
+        B_.spec_profile_set_events(k0, k1)
+        s0.record(stream)
+        B_.spec_draft_sample(h, w, T, 1005, (100 + i) * M, q, x, ws, stream=stream)
+        s1.record(stream)
+    B_.spec_profile_set_events(None, None)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = statistics.mean(a.elapsed_time(b) for a, b, _, _ in ev)
+    gms = statistics.mean(c.elapsed_time(e) for _, _, c, e in ev)
+    peak, peak_kind = _peaks()
+    tpk, tpk_kind = _peak_tflops()
+    gemm_bytes = V * d * 2 + M * d * 2 + M * V * 4  # W, hidden, fp32 logits written
+    flops = 2 * M * d * V
+    finish_bytes = 2 * M * V * 4                     # logits read, q written
+    line = {
+        "metric": "drafted tokens/s (draft head GEMM + q + Philox draw)", "value": M / (ms * 1e-3),
+        "unit": "drafted tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"draft head M={M} d={d} V={V} T={T} bf16 weights, fp32 q",
+                   "l2": "inputs 525 MB > L2, no flush"},
+        "roofline": {"kernel": "lmhead_gemm_kernel (draft head)", "bound": "hbm",
+                     "achieved": gemm_bytes / (gms * 1e-3) / 1e9, "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": gemm_bytes / (gms * 1e-3) / 1e9 / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": gemm_bytes, "ms_per_launch": gms,
+                     "tensor": {"achieved_tflops": flops / (gms * 1e-3) / 1e12, "peak_tflops": tpk,
+                                "peak_kind": tpk_kind, "frac": flops / (gms * 1e-3) / 1e12 / tpk}},
+        "finish": {"ms": ms - gms, "algorithmic_bytes": finish_bytes,
+                   "achieved_gbs": finish_bytes / ((ms - gms) * 1e-3) / 1e9},
+        "clocks": clk, "gpu_launches": 2 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -701,7 +767,7 @@ def main():
     ap.add_argument("--l2-flush", action="store_true",
                     help="write a 256 MB buffer before every timed step (its dirty lines are written back "
                          "during the next step); by default the inputs, larger than L2, stand in for a flush")
-    ap.add_argument("--config", choices=["sampling", "lmhead", "greedy", "ragged", "tiny", "kv"], default="sampling",
+    ap.add_argument("--config", choices=["sampling", "lmhead", "greedy", "ragged", "tiny", "kv", "draft"], default="sampling",
                     help="sampling: the headline workload; lmhead: the fused LM-head front end; "
                          "greedy / ragged / tiny: the other verification workloads")
     args = ap.parse_args()
@@ -713,6 +779,8 @@ def main():
         return run_config(args)
     if args.config == "kv":
         return run_kv(args)
+    if args.config == "draft":
+        return run_draft(args)
     return run_ours(args)
 
 

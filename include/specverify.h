@@ -167,6 +167,35 @@ sv_status spec_lmhead_verify(const void *hidden, const void *w_vocab_t, int d, c
                              float *diag, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * Draft side, the step before verification: q = softmax(h . W / T) over the
+ * vocabulary and one drafted token x ~ q per row ("Speculative Decoding in
+ * Large Language Models", section 2: the draft proposes x ~ q, which the
+ * verification's law assumes; a draft head is read as one linear layer over
+ * the vocabulary).  The logits come from the same tcgen05 GEMM as
+ * spec_lmhead_verify and are written into q_out, which a second kernel turns
+ * into q in place; x is the smallest v with sum_{w<=v} q(w) > u sum_w q(w),
+ * else (rounding) the largest v with q(v) > 0.
+ *   hidden     M x d bf16, row-major, 16-byte aligned; 1 <= M <= 128
+ *   w_vocab_t  V x d bf16 (row v = the weights of token v), 16-byte aligned;
+ *              d a multiple of 64; V a multiple of 4, V <= 1048576
+ *   temperature > 0: sampling (q_out required, 16-byte aligned, M x V fp32);
+ *              0: greedy drafting, x = argmax (lowest index on ties), q_out
+ *              may be NULL and is not written
+ *   seed, offset: row r draws the uniform of Philox4x32-10 (Salmon et al.,
+ *              SC 2011) at counter (offset + r low word, 1, offset + r high
+ *              word, 0) and key (seed low word, seed high word): u = ((w0 >>
+ *              9) + 1/2) 2^-23, w0 its first output word; u_out (M, may be
+ *              NULL) receives it
+ *   x_out      M int32
+ *   ws         spec_draft_workspace_size(M, d, V) bytes, 256-byte aligned
+ * Two kernels on `stream`; argument errors return before any launch.
+ */
+size_t spec_draft_workspace_size(int M, int d, int V);
+sv_status spec_draft_sample(const void *hidden, const void *w_vocab_t, int d, int M, int V,
+                            float temperature, uint64_t seed, uint64_t offset, float *q_out,
+                            int32_t *x_out, float *u_out, void *ws, size_t ws_bytes, void *stream);
+
+/*
  * spec_verify_sample for callers that cannot allocate device memory.  The
  * pages have no counterpart to this call; it exists for host programs with
  * no allocator to hand, e.g. a plugin inside an inference server whose

@@ -26,6 +26,7 @@ EXPORTS = (
     "spec_lmhead_workspace_size", "spec_lmhead_verify", "spec_verify_last_device_status",
     "spec_status_string", "spec_profile_set_events", "spec_last_launch_count",
     "spec_verify_sample_noalloc", "spec_set_small_kernel_limit", "spec_kv_reserve", "spec_kv_rollback",
+    "spec_draft_workspace_size", "spec_draft_sample",
 )
 
 _lock = threading.Lock()
@@ -68,6 +69,8 @@ def load() -> ctypes.CDLL:
             "spec_set_small_kernel_limit": (Z, [Z]),
             "spec_kv_reserve": (I, [P, P, P, P, P, I, I, I, P, P]),
             "spec_kv_rollback": (I, [P, P, P, P, P, P, I, I, I, I, P, P]),
+            "spec_draft_workspace_size": (Z, [I, I, I]),
+            "spec_draft_sample": (I, [P, P, I, I, I, F, ctypes.c_uint64, ctypes.c_uint64, P, P, P, P, Z, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -290,6 +293,28 @@ def spec_kv_rollback(block_table, seq_len, free_ids, free_count, n_spec, accept_
                                  _ptr(accept_len), B, max_blocks, int(block_size), free_ids.numel(), _ptr(status),
                                  _stream(stream))
     _raise(st, "spec_kv_rollback")
+
+
+def spec_draft_workspace_size(M: int, d: int, V: int) -> int:
+    return int(load().spec_draft_workspace_size(M, d, V))
+
+
+def spec_draft_sample(hidden, w_vocab_t, temperature, seed, offset, q_out, x_out, ws, u_out=None, stream=None):
+    """Draft head + sampling: q_out (M, V) fp32 (sampling) and x_out (M,) int32."""
+    _check(hidden, torch.bfloat16, None, "hidden")
+    _check(w_vocab_t, torch.bfloat16, None, "w_vocab_t")
+    M, d = hidden.shape
+    V = w_vocab_t.shape[0]
+    if w_vocab_t.shape[1] != d:
+        raise ValueError("w_vocab_t: expected (V, d)")
+    _check(x_out, torch.int32, M, "x_out")
+    if temperature > 0:
+        _check(q_out, torch.float32, M * V, "q_out")
+    _check(u_out, torch.float32, M, "u_out")
+    st = load().spec_draft_sample(_ptr(hidden), _ptr(w_vocab_t), d, M, V, float(temperature),
+                                  int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(q_out), _ptr(x_out),
+                                  _ptr(u_out), _ptr(ws), ws.numel(), _stream(stream))
+    _raise(st, "spec_draft_sample")
 
 
 def spec_last_launch_count() -> int:

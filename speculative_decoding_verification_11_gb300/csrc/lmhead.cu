@@ -32,6 +32,7 @@
 
 #include "../../include/specverify.h"
 #include "sv_device.cuh"
+#include "sv_draw.cuh"
 #include "sv_host.h"
 
 namespace sv {
@@ -425,6 +426,182 @@ static void launch_gemm_bn(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
     }
 }
 
+// ---------------------------------------------------------------------------
+// Draft sampling (the step before verification): q = softmax(h . W / T) and
+// x ~ q for every draft row.  The GEMM above writes the fp32 logits straight
+// into the caller's q buffer and one (M, S) partial per row and CTA; then one
+// CTA per row merges the partials, turns the row into q in place and draws x
+// by inverse CDF with a Philox4x32-10 uniform.
+// ---------------------------------------------------------------------------
+constexpr int kDraftThreads = 1024;
+constexpr int kDraftWarps = kDraftThreads / 32;
+constexpr int kMaxDraftSegs = 4096;  // V <= 4096 x 256 tokens
+constexpr uint32_t kDraftStream = 1;  // Philox stream of the draft draws
+
+// First output word of Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel
+// random numbers: as easy as 1, 2, 3", SC 2011) at counter (index low word,
+// stream, index high word, 0) and key (seed low word, seed high word).
+__device__ __forceinline__ uint32_t philox_w0(uint64_t seed, uint64_t index, uint32_t stream) {
+    uint32_t c0 = static_cast<uint32_t>(index), c1 = stream, c2 = static_cast<uint32_t>(index >> 32), c3 = 0u;
+    uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    return c0;
+}
+
+// u = ((w0 >> 9) + 1/2) 2^-23, exact in fp32, in (0, 1).
+__device__ __forceinline__ float philox_uniform(uint64_t seed, uint64_t index, uint32_t stream) {
+    const uint32_t w = philox_w0(seed, index, stream);
+    return __fmul_rn(__fadd_rn(__uint2float_rn(w >> 9), 0.5f), 1.0f / 8388608.0f);
+}
+
+template <bool kSample>
+__global__ void __launch_bounds__(kDraftThreads) draft_finish_kernel(float *q, const float2 *partials, int n_parts,
+                                                                     int V, float c, uint64_t seed, uint64_t offset,
+                                                                     int32_t *x_out, float *u_out) {
+    pdl_wait_prior_grid();  // the logits and partials come from the GEMM before it
+    pdl_launch_dependents();
+    const int row = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    __shared__ float2 s_part[kDraftWarps];
+    __shared__ float s_segsum[kMaxDraftSegs];
+    __shared__ DS s_wtot[kDraftWarps];
+    __shared__ int s_owner, s_vstar;
+    __shared__ float s_u;
+
+    // merge the row's partials in a fixed order (per warp, then warp 0 over the warps)
+    float ra;
+    int rb;
+    partial_identity<kSample>(ra, rb);
+    for (int i = tid; i < n_parts; i += kDraftThreads)
+        merge_pair<kSample>(ra, rb, partials[static_cast<size_t>(row) * n_parts + i]);
+    warp_partial_reduce<kSample>(ra, rb);
+    if (lane == 0) s_part[warp] = make_float2(ra, __int_as_float(rb));
+    if (tid == 0) {
+        s_owner = 0x7fffffff;
+        s_vstar = -1;
+        s_u = kSample ? philox_uniform(seed, offset + static_cast<uint64_t>(row), kDraftStream) : 0.f;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const float2 w = s_part[lane];
+        ra = w.x;
+        rb = __float_as_int(w.y);
+        warp_partial_reduce<kSample>(ra, rb);
+        if (lane == 0) s_part[0] = make_float2(ra, __int_as_float(rb));
+    }
+    __syncthreads();
+    if (!kSample) {  // greedy drafting: the argmax
+        if (tid == 0) x_out[row] = __float_as_int(s_part[0].y);
+        return;
+    }
+    const float M = s_part[0].x, invS = 1.f / s_part[0].y;
+    const float u = s_u;
+    float *qrow = q + static_cast<size_t>(row) * V;
+    const int ns = (V + kSegElems - 1) / kSegElems;
+    const int G = (ns + kDraftWarps - 1) / kDraftWarps;
+    const int g0 = min(warp * G, ns), g1 = min(g0 + G, ns);
+
+    // pass 1: each warp turns its segments into q (in place) and sums them in order
+    DS wt{0.f, 0.f};
+    for (int g = g0; g < g1; ++g) {
+        float r[2][4];
+        seg_load_r<float>(qrow, nullptr, V, g, c, M, invS, lane, r);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int e0 = g * kSegElems + (j * 32 + lane) * 4;
+            if (e0 < V) *reinterpret_cast<float4 *>(qrow + e0) = make_float4(r[j][0], r[j][1], r[j][2], r[j][3]);
+        }
+        const float m = seg_sum(r);
+        if (lane == 0) s_segsum[g] = m;
+        wt = ds_add_f(wt, m);
+    }
+    if (lane == 0) s_wtot[warp] = wt;
+    __syncthreads();
+    DS R{0.f, 0.f}, Pw{0.f, 0.f};
+    for (int w = 0; w < kDraftWarps; ++w) {
+        if (w < warp) Pw = ds_add(Pw, s_wtot[w]);
+        R = ds_add(R, s_wtot[w]);
+    }
+    const DS t = ds_mul_f(R, u);
+    if (lane == 0 && g0 < g1 && !ds_gt(Pw, t) && ds_gt(ds_add(Pw, wt), t)) atomicMin(&s_owner, warp);
+    __syncthreads();
+
+    // the owning warp finds the segment, then the token, in token order
+    if (warp == s_owner) {
+        DS P = Pw, fbase{0.f, 0.f};
+        int fseg = -1;
+        for (int g = g0; g < g1; ++g) {
+            const DS Pn = ds_add_f(P, s_segsum[g]);
+            if (ds_gt(Pn, t)) {
+                fseg = g;
+                fbase = P;
+                break;
+            }
+            P = Pn;
+        }
+        int vstar = -1;
+        if (fseg >= 0) {
+            float r[2][4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int e0 = fseg * kSegElems + (j * 32 + lane) * 4;
+                const float4 w = (e0 < V) ? *reinterpret_cast<const float4 *>(qrow + e0) : make_float4(0.f, 0.f, 0.f, 0.f);
+                r[j][0] = w.x;
+                r[j][1] = w.y;
+                r[j][2] = w.z;
+                r[j][3] = w.w;
+            }
+            vstar = warp_seg_scan(r, fseg, V, fbase, t, lane).v;
+            // sums that end short of u R inside the segment: the next token with q > 0
+            for (int g = fseg + 1; g < ns && vstar < 0; ++g) {
+                int loc = 0x7fffffff;
+#pragma unroll
+                for (int j = 1; j >= 0; --j) {
+                    const int e0 = g * kSegElems + (j * 32 + lane) * 4;
+                    if (e0 < V) {
+                        const float4 w = *reinterpret_cast<const float4 *>(qrow + e0);
+                        if (w.w > 0.f) loc = e0 + 3;
+                        if (w.z > 0.f) loc = e0 + 2;
+                        if (w.y > 0.f) loc = e0 + 1;
+                        if (w.x > 0.f) loc = e0;
+                    }
+                }
+                const int best = __reduce_min_sync(0xffffffffu, loc);
+                if (best != 0x7fffffff) vstar = best;
+            }
+        }
+        if (lane == 0) s_vstar = vstar;
+    }
+    __syncthreads();
+    int vstar = s_vstar;
+    if (vstar < 0) {
+        // u R at or above every boundary: the last token with q > 0
+        for (int v = V - 1 - tid; v >= 0; v -= kDraftThreads)
+            if (qrow[v] > 0.f) {
+                atomicMax(&s_vstar, v);
+                break;
+            }
+        __syncthreads();
+        vstar = s_vstar;
+    }
+    if (tid == 0) {
+        x_out[row] = vstar;
+        if (u_out) u_out[row] = u;
+    }
+}
+
 }  // namespace lm
 }  // namespace sv
 
@@ -487,4 +664,72 @@ extern "C" sv_status spec_lmhead_verify(const void *hidden, const void *w_vocab_
                                               &more);
     set_launches(1 + more);
     return st;
+}
+
+// Workspace of spec_draft_sample: a status word, then one partial per row and
+// GEMM CTA.
+extern "C" size_t spec_draft_workspace_size(int M, int d, int V) {
+    (void)d;
+    (void)V;
+    if (M <= 0) return 256;
+    return 256 + lm::a256(sizeof(float2) * static_cast<size_t>(M) * lm::kMaxLmGrid);
+}
+
+extern "C" sv_status spec_draft_sample(const void *hidden, const void *w_vocab_t, int d, int M, int V,
+                                       float temperature, uint64_t seed, uint64_t offset, float *q_out,
+                                       int32_t *x_out, float *u_out, void *ws, size_t ws_bytes, void *stream) {
+    if (M < 0 || M > lm::BM || V <= 0 || V % 4 != 0 || V > lm::kMaxDraftSegs * kSegElems || d < lm::BK ||
+        d % lm::BK != 0 || !(temperature >= 0.f) || !std::isfinite(temperature))
+        return SV_ERR_INVALID;
+    if (M == 0) {
+        set_launches(0);
+        return SV_OK;
+    }
+    const bool sample = temperature > 0.f;
+    if (!hidden || !w_vocab_t || !x_out || !ws || (sample && !q_out)) return SV_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(hidden) & 15u) || (reinterpret_cast<uintptr_t>(w_vocab_t) & 15u) ||
+        (sample && (reinterpret_cast<uintptr_t>(q_out) & 15u)))
+        return SV_ERR_INVALID;
+    if (ws_bytes < spec_draft_workspace_size(M, d, V) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return SV_ERR_WORKSPACE;
+    const int bn = lm::choose_bn(V, sm_count());
+    const int n_tiles = (V + bn - 1) / bn;
+    int grid = n_tiles < sm_count() ? n_tiles : sm_count();
+    if (grid > lm::kMaxLmGrid) grid = lm::kMaxLmGrid;
+    CUtensorMap ta, tb;
+    if (!lm::encode_bf16_kmajor(&ta, hidden, M, d, lm::BM) || !lm::encode_bf16_kmajor(&tb, w_vocab_t, V, d, bn))
+        return SV_ERR_CUDA;
+    char *w = static_cast<char *>(ws);
+    lm::LmArgs a;
+    a.M = M;
+    a.d = d;
+    a.V = V;
+    a.n_tiles = n_tiles;
+    a.c = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(temperature)) : 1.f;
+    a.spill = sample ? q_out : nullptr;  // the logits land in q's buffer, turned into q in place
+    a.partials = reinterpret_cast<float2 *>(w + 256);
+    a.status = reinterpret_cast<uint32_t *>(w);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    prof_begin(s);
+    if (sample) lm::launch_gemm_bn<true>(bn, ta, tb, a, grid, s);
+    else lm::launch_gemm_bn<false>(bn, ta, tb, a, grid, s);
+    prof_end(s);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(M);
+    cfg.blockDim = dim3(lm::kDraftThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = sample ? cudaLaunchKernelEx(&cfg, lm::draft_finish_kernel<true>, q_out,
+                                                      static_cast<const float2 *>(a.partials), grid, V, a.c, seed,
+                                                      offset, x_out, u_out)
+                                 : cudaLaunchKernelEx(&cfg, lm::draft_finish_kernel<false>, q_out,
+                                                      static_cast<const float2 *>(a.partials), grid, V, a.c, seed,
+                                                      offset, x_out, u_out);
+    set_launches(2);
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

@@ -29,6 +29,7 @@
 
 #include "../../include/specverify.h"
 #include "sv_device.cuh"
+#include "sv_draw.cuh"
 #include "sv_host.h"
 
 namespace sv {
@@ -121,27 +122,7 @@ __device__ __forceinline__ float logit_at(const Args &a, size_t i) {
     return Elem<T>::at(reinterpret_cast<const T *>(a.logits), i);
 }
 
-template <bool kSample>
-__device__ __forceinline__ void warp_partial_reduce(float &ra, int &rb) {
-    if (kSample) {
-        float s = __int_as_float(rb);
-        warp_ms_reduce(ra, s);
-        rb = __float_as_int(s);
-    } else {
-        warp_am_reduce(ra, rb);
-    }
-}
 
-template <bool kSample>
-__device__ __forceinline__ void merge_pair(float &ra, int &rb, float2 w) {
-    if (kSample) {
-        float s = __int_as_float(rb);
-        ms_merge(ra, s, w.x, w.y);
-        rb = __float_as_int(s);
-    } else {
-        am_merge(ra, rb, w.x, __float_as_int(w.y));
-    }
-}
 
 // ---------------------------------------------------------------------------
 // Decide step of request b, run by one warp once every chunk partial of the
@@ -397,11 +378,6 @@ __device__ __forceinline__ void lane_accumulate(const float (&vals)[NV][VEC], co
     }
 }
 
-template <bool kSample>
-__device__ __forceinline__ void partial_identity(float &ra, int &rb) {
-    ra = -INFINITY;
-    rb = kSample ? __float_as_int(0.f) : 0x7fffffff;
-}
 
 // ---------------------------------------------------------------------------
 // Pass 1, any alignment: one CTA per (row, chunk), element loads.
@@ -536,11 +512,6 @@ __device__ __forceinline__ void warp_tile_compute(const TileRaw<T> &raw, bool ha
     }
 }
 
-struct TileScan {
-    int v;       // found token (kFind) or -1
-    float rv;    // its r(v)
-    float mass;  // tile mass
-};
 
 // kFind = false: tile mass (valid in every lane).
 // kFind = true : the smallest token v < V of the tile with base + E(v) > t
@@ -921,127 +892,6 @@ __device__ __forceinline__ float res_lane_sum(const unsigned char *stage, int wa
     return acc;
 }
 
-// r(v) of the 8 tokens a lane holds in 256-token segment g of a row: token
-// g * 256 + (j * 32 + lane) * 4 + k, j < 2, k < 4; zero beyond V.  Same
-// arithmetic as res_lane_sum (V is a multiple of 4 on this path).
-template <typename T>
-__device__ __forceinline__ void seg_load_r(const T *zrow, const float *qrow, int V, int g, float c, float M,
-                                           float invS, int lane, float (&r)[2][4]) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int e0 = g * kSegElems + (j * 32 + lane) * 4;
-        float z[4] = {0.f, 0.f, 0.f, 0.f}, qv[4] = {0.f, 0.f, 0.f, 0.f};
-        const bool in = e0 < V;
-        if (in) {
-            if constexpr (sizeof(T) == 4) {
-                const float4 w = __ldcs(reinterpret_cast<const float4 *>(zrow + e0));
-                z[0] = w.x; z[1] = w.y; z[2] = w.z; z[3] = w.w;
-            } else {
-                const uint2 w = __ldcs(reinterpret_cast<const uint2 *>(zrow + e0));
-                z[0] = __uint_as_float(w.x << 16);
-                z[1] = __uint_as_float(w.x & 0xffff0000u);
-                z[2] = __uint_as_float(w.y << 16);
-                z[3] = __uint_as_float(w.y & 0xffff0000u);
-            }
-            if (qrow) {
-                const float4 w = __ldcs(reinterpret_cast<const float4 *>(qrow + e0));
-                qv[0] = w.x; qv[1] = w.y; qv[2] = w.z; qv[3] = w.w;
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float p = __fmul_rn(ex2(__fmaf_rn(z[k], c, -M)), invS);
-            r[j][k] = in ? (qrow ? fmaxf(__fsub_rn(p, qv[k]), 0.f) : p) : 0.f;
-        }
-    }
-}
-
-// Double-single arithmetic: an unevaluated sum hi + lo of two fp32 values
-// (about 48 significant bits), from error-free transformations (Knuth's
-// TwoSum; the product error from one fma).  FP64 runs at a small fraction of
-// the fp32 rate on this GPU, and the draw's prefix sums sit on the critical
-// path, so they are kept in this form instead.
-struct DS {
-    float hi, lo;
-};
-__device__ __forceinline__ DS ds_two_sum(float a, float b) {
-    const float s = __fadd_rn(a, b);
-    const float bb = __fsub_rn(s, a);
-    const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-    return DS{s, e};
-}
-__device__ __forceinline__ DS ds_norm(float s, float e) {
-    const float hi = __fadd_rn(s, e);
-    return DS{hi, __fsub_rn(e, __fsub_rn(hi, s))};
-}
-__device__ __forceinline__ DS ds_add(DS a, DS b) {
-    const DS t = ds_two_sum(a.hi, b.hi);
-    return ds_norm(t.hi, __fadd_rn(t.lo, __fadd_rn(a.lo, b.lo)));
-}
-__device__ __forceinline__ DS ds_add_f(DS a, float b) {
-    const DS t = ds_two_sum(a.hi, b);
-    return ds_norm(t.hi, __fadd_rn(t.lo, a.lo));
-}
-__device__ __forceinline__ DS ds_mul_f(DS a, float b) {
-    const float p = __fmul_rn(a.hi, b);
-    const float e = __fmaf_rn(a.lo, b, __fmaf_rn(a.hi, b, -p));
-    return ds_norm(p, e);
-}
-// a > b
-__device__ __forceinline__ bool ds_gt(DS a, DS b) {
-    const DS d = ds_add(a, DS{-b.hi, -b.lo});
-    return d.hi > 0.f || (d.hi == 0.f && d.lo > 0.f);
-}
-__device__ __forceinline__ DS ds_shfl_up(DS a, int o) {
-    return DS{__shfl_up_sync(0xffffffffu, a.hi, o), __shfl_up_sync(0xffffffffu, a.lo, o)};
-}
-__device__ __forceinline__ DS ds_shfl(DS a, int src) {
-    return DS{__shfl_sync(0xffffffffu, a.hi, src), __shfl_sync(0xffffffffu, a.lo, src)};
-}
-
-// Running sums of a segment in token order (fp32 within the segment, on top
-// of the double-single prefix base_p of the segments before it): the first
-// token whose running sum passes t, or -1.
-__device__ __forceinline__ TileScan warp_seg_scan(const float (&r)[2][4], int g, int V, DS base_p, DS t, int lane) {
-    float base = 0.f;
-    TileScan res{-1, 0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        float pre[4];
-        pre[0] = r[j][0];
-        pre[1] = __fadd_rn(pre[0], r[j][1]);
-        pre[2] = __fadd_rn(pre[1], r[j][2]);
-        pre[3] = __fadd_rn(pre[2], r[j][3]);
-        float incl = pre[3];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl = __fadd_rn(incl, y);
-        }
-        float lex = __shfl_up_sync(0xffffffffu, incl, 1);
-        if (lane == 0) lex = 0.f;
-        const float seg = __shfl_sync(0xffffffffu, incl, 31);
-        const float head = __fadd_rn(base, lex);
-        int cand = -1;
-        const int e0 = g * kSegElems + (j * 32 + lane) * 4;
-#pragma unroll
-        for (int k = 3; k >= 0; --k)
-            if (e0 + k < V && ds_gt(ds_add_f(base_p, __fadd_rn(head, pre[k])), t)) cand = k;
-        const unsigned m = __ballot_sync(0xffffffffu, cand >= 0);
-        if (m && res.v < 0) {
-            const int src = __ffs(m) - 1;
-            const int ck = __shfl_sync(0xffffffffu, cand, src);
-            float rsel = 0.f;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (k == ck) rsel = r[j][k];
-            res.v = g * kSegElems + (j * 32 + src) * 4 + ck;
-            res.rv = __shfl_sync(0xffffffffu, rsel, src);
-        }
-        base = __fadd_rn(base, seg);
-    }
-    return res;
-}
 
 struct Sel {
     int valid;   // 0: an invalid draft id (nothing to draw)
@@ -1191,13 +1041,6 @@ __device__ bool fused_decide(const Args &a, int b, int lane, volatile int *abort
     return true;
 }
 
-// Sum of a segment's r(v) in a fixed order (the slow path below uses it twice).
-__device__ __forceinline__ float seg_sum(const float (&r)[2][4]) {
-    float m = ((r[0][0] + r[0][1]) + (r[0][2] + r[0][3])) + ((r[1][0] + r[1][1]) + (r[1][2] + r[1][3]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
-    return m;
-}
 
 // Final draw of request b by its owning worker warp, once every segment mass
 // of the selected row is in: an fp64 prefix over the segments, then running
@@ -1703,7 +1546,7 @@ __global__ void __launch_bounds__(kThreads) small_kernel(Args a, int nr_cap) {
     T *zs = reinterpret_cast<T *>(smem);
     float2 *st = reinterpret_cast<float2 *>(smem + a16(static_cast<size_t>(nr_cap) * V * sizeof(T)));
     float *rr = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(st) + a16(static_cast<size_t>(nr_cap) * 8));
-    fz::DS *ts = reinterpret_cast<fz::DS *>(reinterpret_cast<unsigned char *>(rr) + a16(static_cast<size_t>(V) * 4));
+    DS *ts = reinterpret_cast<DS *>(reinterpret_cast<unsigned char *>(rr) + a16(static_cast<size_t>(V) * 4));
     __shared__ int s_bad, s_ks, s_best;
 
     // drafts of the first 32 rows: their gathers are in flight during the copy
@@ -1818,41 +1661,41 @@ __global__ void __launch_bounds__(kThreads) small_kernel(Args a, int nr_cap) {
     const float uK = __ldg(a.uniforms + r0 + Kb);
     const int L = (V + kThreads - 1) / kThreads;
     const int v0 = min(tid * L, V), v1 = min(v0 + L, V);
-    fz::DS P{0.f, 0.f}, incl{0.f, 0.f}, R{0.f, 0.f};
+    DS P{0.f, 0.f}, incl{0.f, 0.f}, R{0.f, 0.f};
     for (int attempt = 0; attempt < 2; ++attempt) {
-        fz::DS sum{0.f, 0.f};
+        DS sum{0.f, 0.f};
         for (int v = v0; v < v1; ++v) {
             const float p = __fmul_rn(ex2(__fmaf_rn(to_f<T>(zr[v]), a.c, -M)), invS);
             const float r = qrow ? fmaxf(__fsub_rn(p, __ldg(qrow + v)), 0.f) : p;
             rr[v] = r;
-            sum = fz::ds_add_f(sum, r);
+            sum = ds_add_f(sum, r);
         }
         // block-wide inclusive scan of the per-thread sums (double-single)
         incl = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const fz::DS y = fz::ds_shfl_up(incl, o);
-            if (lane >= o) incl = fz::ds_add(incl, y);
+            const DS y = ds_shfl_up(incl, o);
+            if (lane >= o) incl = ds_add(incl, y);
         }
         if (lane == 31) ts[warp] = incl;
         __syncthreads();
-        fz::DS wpre{0.f, 0.f};
-        for (int w = 0; w < warp; ++w) wpre = fz::ds_add(wpre, ts[w]);
+        DS wpre{0.f, 0.f};
+        for (int w = 0; w < warp; ++w) wpre = ds_add(wpre, ts[w]);
         R = ts[0];
-        for (int w = 1; w < kWarps; ++w) R = fz::ds_add(R, ts[w]);
-        incl = fz::ds_add(wpre, incl);
-        P = fz::ds_add(incl, fz::DS{-sum.hi, -sum.lo});
+        for (int w = 1; w < kWarps; ++w) R = ds_add(R, ts[w]);
+        incl = ds_add(wpre, incl);
+        P = ds_add(incl, DS{-sum.hi, -sum.lo});
         __syncthreads();
         if (R.hi > 0.f || attempt == 1) break;
         // empty residual after a rejection: draw from p instead
         qrow = nullptr;
         if (tid == 0) atomicOr(a.status, SV_FLAG_ZERO_RESIDUAL);
     }
-    const fz::DS t = fz::ds_mul_f(R, uK);
+    const DS t = ds_mul_f(R, uK);
     // the first thread whose run holds u R scans it in token order
     if (tid == 0) s_best = 0x7fffffff;
     __syncthreads();
-    const bool holds = v0 < v1 && fz::ds_gt(incl, t) && !fz::ds_gt(P, t);
+    const bool holds = v0 < v1 && ds_gt(incl, t) && !ds_gt(P, t);
     if (holds) atomicMin(&s_best, tid);
     __syncthreads();
     const int owner = s_best;
@@ -1860,11 +1703,11 @@ __global__ void __launch_bounds__(kThreads) small_kernel(Args a, int nr_cap) {
     if (tid == 0) s_best = 0x7fffffff;  // reused below: the drawn token
     __syncthreads();
     if (tid == owner) {
-        fz::DS run = P;
+        DS run = P;
         int vs = -1;
         for (int v = v0; v < v1; ++v) {
-            run = fz::ds_add_f(run, rr[v]);
-            if (fz::ds_gt(run, t)) {
+            run = ds_add_f(run, rr[v]);
+            if (ds_gt(run, t)) {
                 vs = v;
                 break;
             }
