@@ -17,6 +17,9 @@ Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``
   kv_blocks.*              pinned: token-by-token simulation, conservation of
                            block ids, reserve + full rejection = identity,
                            K - M evictions (tests/test_oracle_pins_kv.py).
+  ngram.*                  pinned: str.rfind over an encoding of the tokens,
+                           a periodic stream's closed form, special cases
+                           (tests/test_oracle_pins_ngram.py).
   draft.*                  pinned: Philox4x32-10 known-answer vectors, exact
                            rational enumeration of the draw, chi-square of the
                            draws (tests/test_oracle_pins_draft.py).
