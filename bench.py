@@ -757,6 +757,62 @@ def run_draft(args):
     return 0
 
 
+def run_ngram(args):
+    """Model-free n-gram (prompt lookup) drafting over synthetic streams with
+    repetition: B = 256 contexts of L tokens (L = 8192 and 32768), K = 8,
+    n in [1, 4].  The contexts fit in L2, so every call is preceded by a
+    256 MB write then a 256 MB read, outside its events."""
+    import torch
+    from speculative_decoding_verification_11_gb300 import build, binding as B_, workloads as W
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    fw = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    fr = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    res = {}
+    B, K, n_min, n_max = 256, 8, 1, 4
+    for L in (8192, 32768):
+        tokens, offs = W.repetitive_streams(seed=1006, B=B, L=L)
+        t = torch.from_numpy(tokens).to(dev)
+        o = torch.from_numpy(offs).to(dev)
+        d = torch.empty(B, K, dtype=torch.int32, device=dev)
+        k = torch.empty(B, dtype=torch.int32, device=dev)
+        for _ in range(max(args.warmup, 3)):
+            B_.spec_ngram_draft(t, o, K, n_min, n_max, d, k, stream=stream)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            fw.fill_(float(i))
+            fr.sum()
+            ev[i][0].record(stream)
+            B_.spec_ngram_draft(t, o, K, n_min, n_max, d, k, stream=stream)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        kh = k.cpu()
+        alg = B * L * 4 + (B + 1) * 4 + B * K * 4 + B * 4
+        res[f"L={L}"] = {"us_per_call": ms * 1e3, "requests_per_s": B / (ms * 1e-3),
+                         "mean_draft_len": float(kh.float().mean()), "with_proposal": float((kh > 0).float().mean()),
+                         "algorithmic_bytes": alg, "achieved_gbs": alg / (ms * 1e-3) / 1e9}
+    peak, peak_kind = _peaks()
+    head = res["L=8192"]
+    line = {
+        "metric": "n-gram drafting requests/s", "value": head["requests_per_s"], "unit": "requests/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": head["us_per_call"] * 1e-3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": {"workload": f"prompt-lookup drafting B={B} K={K} n={n_min}..{n_max} over repetitive streams",
+                   "l2": "contexts < L2: 256 MB write then 256 MB read before every call, outside its events"},
+        "roofline": {"kernel": "ng::ngram_kernel", "bound": "hbm", "achieved": head["achieved_gbs"], "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": head["achieved_gbs"] / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": head["algorithmic_bytes"],
+                     "ms_per_launch": head["us_per_call"] * 1e-3},
+        "lengths": res, "gpu_launches": 2 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -767,7 +823,7 @@ def main():
     ap.add_argument("--l2-flush", action="store_true",
                     help="write a 256 MB buffer before every timed step (its dirty lines are written back "
                          "during the next step); by default the inputs, larger than L2, stand in for a flush")
-    ap.add_argument("--config", choices=["sampling", "lmhead", "greedy", "ragged", "tiny", "kv", "draft"], default="sampling",
+    ap.add_argument("--config", choices=["sampling", "lmhead", "greedy", "ragged", "tiny", "kv", "draft", "ngram"], default="sampling",
                     help="sampling: the headline workload; lmhead: the fused LM-head front end; "
                          "greedy / ragged / tiny: the other verification workloads")
     args = ap.parse_args()
@@ -781,6 +837,8 @@ def main():
         return run_kv(args)
     if args.config == "draft":
         return run_draft(args)
+    if args.config == "ngram":
+        return run_ngram(args)
     return run_ours(args)
 
 

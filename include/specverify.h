@@ -196,6 +196,23 @@ sv_status spec_draft_sample(const void *hidden, const void *w_vocab_t, int d, in
                             int32_t *x_out, float *u_out, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * Model-free n-gram (prompt lookup) drafter ("Co-Designing AI Models Using
+ * Speculative Decoding for Faster LLM Inference", Table 1: suffix / n-gram
+ * drafting matches strings over the token stream, no model, one lookup).
+ * Request b's context is tokens[ctx_offsets[b] .. ctx_offsets[b+1]) (int32,
+ * CSR, device).  For n = n_max down to n_min, the context's last n tokens are
+ * looked up among earlier windows that end before its last token; at the
+ * first n with a match, the latest such window wins and the up to K tokens
+ * that follow it are proposed (fewer when the context ends first).  Outputs:
+ * draft_out [B x K] int32 (-1 past the proposal), k_out [B] (0..K: the draft
+ * length each request proposes, e.g. the K_b of spec_verify_ragged).
+ * 1 <= n_min <= n_max <= 32, 0 <= K <= SV_MAX_K.  One kernel on `stream`; a
+ * request whose offsets decrease proposes nothing.
+ */
+sv_status spec_ngram_draft(const int32_t *tokens, const int32_t *ctx_offsets, int B, int K, int n_min,
+                           int n_max, int32_t *draft_out, int32_t *k_out, void *stream);
+
+/*
  * spec_verify_sample for callers that cannot allocate device memory.  The
  * pages have no counterpart to this call; it exists for host programs with
  * no allocator to hand, e.g. a plugin inside an inference server whose

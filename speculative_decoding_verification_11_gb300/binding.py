@@ -26,7 +26,7 @@ EXPORTS = (
     "spec_lmhead_workspace_size", "spec_lmhead_verify", "spec_verify_last_device_status",
     "spec_status_string", "spec_profile_set_events", "spec_last_launch_count",
     "spec_verify_sample_noalloc", "spec_set_small_kernel_limit", "spec_kv_reserve", "spec_kv_rollback",
-    "spec_draft_workspace_size", "spec_draft_sample",
+    "spec_draft_workspace_size", "spec_draft_sample", "spec_ngram_draft",
 )
 
 _lock = threading.Lock()
@@ -71,6 +71,7 @@ def load() -> ctypes.CDLL:
             "spec_kv_rollback": (I, [P, P, P, P, P, P, I, I, I, I, P, P]),
             "spec_draft_workspace_size": (Z, [I, I, I]),
             "spec_draft_sample": (I, [P, P, I, I, I, F, ctypes.c_uint64, ctypes.c_uint64, P, P, P, P, Z, P]),
+            "spec_ngram_draft": (I, [P, P, I, I, I, I, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -315,6 +316,18 @@ def spec_draft_sample(hidden, w_vocab_t, temperature, seed, offset, q_out, x_out
                                   int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(q_out), _ptr(x_out),
                                   _ptr(u_out), _ptr(ws), ws.numel(), _stream(stream))
     _raise(st, "spec_draft_sample")
+
+
+def spec_ngram_draft(tokens, ctx_offsets, K, n_min, n_max, draft_out, k_out, stream=None):
+    """Prompt-lookup drafts: draft_out (B, K) int32 (-1 padded), k_out (B,) int32."""
+    _check(tokens, torch.int32, None, "tokens")
+    _check(ctx_offsets, torch.int32, None, "ctx_offsets")
+    B = ctx_offsets.numel() - 1
+    _check(draft_out, torch.int32, B * K, "draft_out")
+    _check(k_out, torch.int32, B, "k_out")
+    st = load().spec_ngram_draft(_ptr(tokens), _ptr(ctx_offsets), B, K, n_min, n_max, _ptr(draft_out), _ptr(k_out),
+                                 _stream(stream))
+    _raise(st, "spec_ngram_draft")
 
 
 def spec_last_launch_count() -> int:

@@ -264,3 +264,30 @@ def nominal_bytes(batch: Batch) -> int:
     lb = batch.rows * batch.V * esize if batch.logits is not None else 0
     qb = batch.n_draft * batch.V * 4 if batch.q is not None else 0
     return lb + qb
+
+
+def repetitive_streams(seed: int = 1006, B: int = 256, L: int = 8192, vocab: int = 32000,
+                       copy_prob: float = 0.05, span=(8, 64)):
+    """Synthetic token streams with repetition, the kind n-gram drafting is for
+    (outputs that copy from their inputs).  Each stream starts with one random
+    token; then, at every position, with probability copy_prob it copies a span
+    of U{span} tokens from a uniformly chosen earlier position, else it emits a
+    uniform random token.  Returns (tokens int32 concatenated, offsets (B+1,)
+    int32)."""
+    rng = np.random.default_rng(seed)
+    out, offs = [], [0]
+    for _ in range(B):
+        s = [int(rng.integers(0, vocab))]
+        while len(s) < L:
+            if len(s) > 1 and rng.random() < copy_prob:
+                n = int(rng.integers(span[0], span[1] + 1))
+                src = int(rng.integers(0, len(s) - 1))
+                for j in range(n):
+                    s.append(s[src + j])
+                    if len(s) >= L:
+                        break
+            else:
+                s.append(int(rng.integers(0, vocab)))
+        out.extend(s[:L])
+        offs.append(offs[-1] + L)
+    return np.asarray(out, dtype=np.int32), np.asarray(offs, dtype=np.int32)

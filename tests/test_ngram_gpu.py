@@ -1,0 +1,67 @@
+"""GPU parity of the n-gram (prompt lookup) drafter (spec_ngram_draft) against
+the oracle (oracle/ngram.py): integer work, so drafts and counts are equal."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import ngram
+from speculative_decoding_verification_11_gb300 import binding as B_, workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu(dev, tokens, offs, K, n_min, n_max):
+    B = len(offs) - 1
+    t = torch.from_numpy(np.ascontiguousarray(tokens, dtype=np.int32)).to(dev) if len(tokens) else \
+        torch.zeros(1, dtype=torch.int32, device=dev)
+    o = torch.from_numpy(np.asarray(offs, dtype=np.int32)).to(dev)
+    d = torch.full((B, K), -7, dtype=torch.int32, device=dev)
+    k = torch.full((B,), -7, dtype=torch.int32, device=dev)
+    B_.spec_ngram_draft(t, o, K, n_min, n_max, d, k)
+    torch.cuda.synchronize()
+    return d.cpu().numpy(), k.cpu().numpy()
+
+
+def _oracle(tokens, offs, K, n_min, n_max):
+    ctxs = [list(tokens[offs[b]:offs[b + 1]]) for b in range(len(offs) - 1)]
+    d, k = ngram.propose_batch(ctxs, K, n_min, n_max)
+    return np.asarray(d, dtype=np.int32).reshape(len(ctxs), K), np.asarray(k, dtype=np.int32)
+
+
+@pytest.mark.parametrize("alphabet,K,n_min,n_max", [(2, 4, 1, 3), (5, 8, 2, 4), (50, 6, 1, 1), (3, 1, 3, 32)])
+def test_random_streams_match_oracle(cuda_device, alphabet, K, n_min, n_max):
+    rng = np.random.default_rng(alphabet * 100 + K)
+    lens = [0, 1, 2, 3] + rng.integers(4, 700, size=60).tolist()
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    tokens = rng.integers(0, alphabet, size=int(offs[-1])).astype(np.int32)
+    d, k = _gpu(cuda_device, tokens, offs, K, n_min, n_max)
+    od, ok = _oracle(tokens, offs, K, n_min, n_max)
+    assert np.array_equal(k, ok) and np.array_equal(d, od)
+
+
+def test_repetitive_streams_workload(cuda_device):
+    tokens, offs = W.repetitive_streams(seed=1006, B=32, L=3000)
+    d, k = _gpu(cuda_device, tokens, offs, 8, 1, 4)
+    od, ok = _oracle(tokens, offs, 8, 1, 4)
+    assert np.array_equal(k, ok) and np.array_equal(d, od)
+    assert (k > 0).mean() > 0.5  # the streams repeat: most requests find a match
+
+
+def test_decreasing_offsets_propose_nothing(cuda_device):
+    tokens = np.array([1, 2, 1, 2, 1, 2], dtype=np.int32)
+    d, k = _gpu(cuda_device, tokens, [0, 6, 2], 3, 1, 2)
+    assert k[0] == 2 and list(d[0]) == [1, 2, -1]
+    assert k[1] == 0 and list(d[1]) == [-1, -1, -1]
+
+
+def test_ngram_argument_errors(cuda_device):
+    dev = cuda_device
+    t = torch.zeros(4, dtype=torch.int32, device=dev)
+    o = torch.tensor([0, 4], dtype=torch.int32, device=dev)
+    d = torch.zeros(1, 2, dtype=torch.int32, device=dev)
+    k = torch.zeros(1, dtype=torch.int32, device=dev)
+    for n_min, n_max in ((0, 2), (3, 2), (1, 33)):
+        with pytest.raises(B_.SpecVerifyError):
+            B_.spec_ngram_draft(t, o, 2, n_min, n_max, d, k)
