@@ -20,6 +20,10 @@ Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``
   ngram.*                  pinned: str.rfind over an encoding of the tokens,
                            a periodic stream's closed form, special cases
                            (tests/test_oracle_pins_ngram.py).
+  dynk.*                   pinned: closed form of E[N], the estimator's
+                           convergence on simulated acceptance, the pages'
+                           window rule, brute-force goodput argmax
+                           (tests/test_oracle_pins_dynk.py).
   draft.*                  pinned: Philox4x32-10 known-answer vectors, exact
                            rational enumeration of the draw, chi-square of the
                            draws (tests/test_oracle_pins_draft.py).
