@@ -813,6 +813,67 @@ def run_ngram(args):
     return 0
 
 
+def run_dynk(args):
+    """Dynamic-K controller after verification (goodput rule, 10-result rings,
+    K in [1, 8], row offsets for the next ragged verification), B = 64 and
+    4096, captured in a CUDA graph (the update is launch-bound)."""
+    import torch
+    from speculative_decoding_verification_11_gb300 import build, binding as B_
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for Bn in (64, 4096):
+        g = torch.Generator().manual_seed(Bn)
+        al = torch.randint(1, 6, (Bn,), generator=g, dtype=torch.int32).to(dev)
+        ku = torch.full((Bn,), 5, dtype=torch.int32, device=dev)
+        hist = torch.zeros(Bn, 10, 2, dtype=torch.int32, device=dev)
+        count = torch.zeros(Bn, dtype=torch.int32, device=dev)
+        kn = torch.empty(Bn, dtype=torch.int32, device=dev)
+        offs = torch.empty(Bn + 1, dtype=torch.int32, device=dev)
+        itl = (10.0 + 1.5 * torch.arange(9, dtype=torch.float32)).to(dev)
+        for _ in range(max(args.warmup, 3)):
+            B_.spec_dynk_update(al, ku, hist, count, B_.SV_DYNK_GOODPUT, 1, 8, kn, itl=itl, row_offsets=offs,
+                                stream=stream)
+        torch.cuda.synchronize()
+        gs = torch.cuda.Stream(dev)
+        gs.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            for _ in range(args.steps):
+                B_.spec_dynk_update(al, ku, hist, count, B_.SV_DYNK_GOODPUT, 1, 8, kn, itl=itl, row_offsets=offs,
+                                    stream=gs)
+        graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / args.steps
+        alg = Bn * (4 * 4 + 10 * 8 + 8) + 9 * 4  # AL, K used, count, k_next; the ring read (and one pair written); offsets
+        res[f"B={Bn}"] = {"us_per_update": us, "algorithmic_bytes": alg, "achieved_gbs": alg / (us * 1e-6) / 1e9,
+                          "mean_k_next": float(kn.float().mean())}
+    peak, peak_kind = _peaks()
+    head = res["B=64"]
+    line = {
+        "metric": "dynamic-K controller updates/s", "value": 1e6 / head["us_per_update"], "unit": "updates/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": head["us_per_update"] * 1e-3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32/f32", "data": "synthetic",
+        "config": {"workload": "goodput rule, W=10, K in [1, 8], B=64 and 4096, offsets for ragged verification",
+                   "l2": "state stays in L2 (launch-bound, one CTA)"},
+        "roofline": {"kernel": "dk::dynk_kernel", "bound": "hbm", "achieved": head["achieved_gbs"], "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": head["achieved_gbs"] / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": head["algorithmic_bytes"],
+                     "ms_per_launch": head["us_per_update"] * 1e-3,
+                     "note": "latency-bound: one CTA per update, in a CUDA graph"},
+        "batches": res, "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -823,7 +884,7 @@ def main():
     ap.add_argument("--l2-flush", action="store_true",
                     help="write a 256 MB buffer before every timed step (its dirty lines are written back "
                          "during the next step); by default the inputs, larger than L2, stand in for a flush")
-    ap.add_argument("--config", choices=["sampling", "lmhead", "greedy", "ragged", "tiny", "kv", "draft", "ngram"], default="sampling",
+    ap.add_argument("--config", choices=["sampling", "lmhead", "greedy", "ragged", "tiny", "kv", "draft", "ngram", "dynk"], default="sampling",
                     help="sampling: the headline workload; lmhead: the fused LM-head front end; "
                          "greedy / ragged / tiny: the other verification workloads")
     args = ap.parse_args()
@@ -839,6 +900,8 @@ def main():
         return run_draft(args)
     if args.config == "ngram":
         return run_ngram(args)
+    if args.config == "dynk":
+        return run_dynk(args)
     return run_ours(args)
 
 

@@ -213,6 +213,38 @@ sv_status spec_ngram_draft(const int32_t *tokens, const int32_t *ctx_offsets, in
                            int n_max, int32_t *draft_out, int32_t *k_out, void *stream);
 
 /*
+ * Dynamic draft length after verification (the third page's "Dynamic
+ * speculative decoding": K adapted to acceptance and hardware, goodput =
+ * AL / ITL, a table extended with live statistics; "Speculative Decoding in
+ * Production: Accelerating LLM Inference via Custom Draft Models", "Production
+ * Failure Modes and Mitigation Strategies", item 1: K from 5 down to 1 or 2
+ * when the average accepted length over the last 10 falls below 1.5).
+ * Per request b (device arrays owned by the caller, zero-filled before the
+ * first call): hist [B x W x 2] int32 = a ring of its last W results
+ * (AL, K used), count [B] = results pushed so far.  Each call pushes
+ * (accept_len[b], k_used[b]) unless accept_len[b] = 0 (an invalid request),
+ * then writes k_next[b]:
+ *   SV_DYNK_WINDOW   k_low if the mean AL over the ring is below `threshold`,
+ *                    else k_high (k_high while the ring is empty);
+ *   SV_DYNK_GOODPUT  alpha = S / (S + F) over the ring, S = sum (AL - 1),
+ *                    F = results with AL - 1 < K (alpha_prior when S + F = 0);
+ *                    E(K) = 1 + alpha + ... + alpha^K; k_next = the K in
+ *                    [k_low, k_high] maximising E(K) / itl[K] (smaller K on
+ *                    ties), itl [k_high + 1] float = the caller's profiled
+ *                    step time (draft + verify) with K drafts.
+ * All decisions in fp32, round to nearest, in the order written.  If
+ * row_offsets [B + 1] is not NULL it receives the CSR offsets of the next
+ * ragged verification: row_offsets[b] = sum_{i<b} (k_next[i] + 1).
+ * One kernel on `stream`.  0 <= k_low <= k_high <= SV_MAX_K, W >= 1.
+ */
+#define SV_DYNK_WINDOW 0
+#define SV_DYNK_GOODPUT 1
+sv_status spec_dynk_update(const int32_t *accept_len, const int32_t *k_used, int32_t *hist, int32_t *count,
+                           int B, int W, int policy, float threshold, int k_low, int k_high,
+                           const float *itl, float alpha_prior, int32_t *k_next, int32_t *row_offsets,
+                           void *stream);
+
+/*
  * spec_verify_sample for callers that cannot allocate device memory.  The
  * pages have no counterpart to this call; it exists for host programs with
  * no allocator to hand, e.g. a plugin inside an inference server whose

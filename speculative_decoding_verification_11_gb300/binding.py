@@ -19,6 +19,7 @@ SV_OK, SV_ERR_INVALID, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, SV_ERR_TIMEOUT, SV_ERR_
 SV_F32, SV_BF16 = 0, 1
 SV_FLAG_BAD_TOKEN, SV_FLAG_BAD_OFFSETS, SV_FLAG_ZERO_RESIDUAL, SV_FLAG_TIMEOUT = 1, 2, 4, 8
 SV_FLAG_KV_OUT_OF_BLOCKS, SV_FLAG_KV_BAD_INPUT = 0x10, 0x20
+SV_DYNK_WINDOW, SV_DYNK_GOODPUT = 0, 1
 SV_MAX_K = 255
 
 EXPORTS = (
@@ -26,7 +27,7 @@ EXPORTS = (
     "spec_lmhead_workspace_size", "spec_lmhead_verify", "spec_verify_last_device_status",
     "spec_status_string", "spec_profile_set_events", "spec_last_launch_count",
     "spec_verify_sample_noalloc", "spec_set_small_kernel_limit", "spec_kv_reserve", "spec_kv_rollback",
-    "spec_draft_workspace_size", "spec_draft_sample", "spec_ngram_draft",
+    "spec_draft_workspace_size", "spec_draft_sample", "spec_ngram_draft", "spec_dynk_update",
 )
 
 _lock = threading.Lock()
@@ -72,6 +73,7 @@ def load() -> ctypes.CDLL:
             "spec_draft_workspace_size": (Z, [I, I, I]),
             "spec_draft_sample": (I, [P, P, I, I, I, F, ctypes.c_uint64, ctypes.c_uint64, P, P, P, P, Z, P]),
             "spec_ngram_draft": (I, [P, P, I, I, I, I, P, P, P]),
+            "spec_dynk_update": (I, [P, P, P, P, I, I, I, F, I, I, P, F, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -328,6 +330,26 @@ def spec_ngram_draft(tokens, ctx_offsets, K, n_min, n_max, draft_out, k_out, str
     st = load().spec_ngram_draft(_ptr(tokens), _ptr(ctx_offsets), B, K, n_min, n_max, _ptr(draft_out), _ptr(k_out),
                                  _stream(stream))
     _raise(st, "spec_ngram_draft")
+
+
+def spec_dynk_update(accept_len, k_used, hist, count, policy, k_low, k_high, k_next, threshold=1.5, itl=None,
+                     alpha_prior=0.5, row_offsets=None, stream=None):
+    """Dynamic K after verification; hist (B, W, 2) int32 and count (B,) int32
+    carry the state between calls."""
+    B = accept_len.numel()
+    _check(accept_len, torch.int32, B, "accept_len")
+    _check(k_used, torch.int32, B, "k_used")
+    _check(hist, torch.int32, None, "hist")
+    _check(count, torch.int32, B, "count")
+    _check(k_next, torch.int32, B, "k_next")
+    _check(itl, torch.float32, None, "itl")
+    _check(row_offsets, torch.int32, B + 1, "row_offsets")
+    if hist.dim() != 3 or hist.shape[0] != B or hist.shape[2] != 2:
+        raise ValueError("hist: expected (B, W, 2)")
+    st = load().spec_dynk_update(_ptr(accept_len), _ptr(k_used), _ptr(hist), _ptr(count), B, hist.shape[1],
+                                 int(policy), float(threshold), int(k_low), int(k_high), _ptr(itl), float(alpha_prior),
+                                 _ptr(k_next), _ptr(row_offsets), _stream(stream))
+    _raise(st, "spec_dynk_update")
 
 
 def spec_last_launch_count() -> int:
