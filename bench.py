@@ -130,6 +130,22 @@ def _dist():
     return world, rank, local
 
 
+def _max_over_ranks(values, device):
+    """Each rank's timings -> the maximum over ranks of each (the slowest rank
+    sets the job's time); a no-op on one rank."""
+    import torch
+    if int(os.environ.get("WORLD_SIZE", "1")) <= 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def _job_value(world, units_per_rank, ms):
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def _cpu_sample(batch, target_s=10.0):
     """The oracle as it stands on a bounded sample of the workload: the first
     16 requests, repeated until ~target_s of host time."""
@@ -147,6 +163,36 @@ def _cpu_sample(batch, target_s=10.0):
             break
     return {"value": reps * n_req * batch.K / el, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"first {n_req} of 64 requests, {reps} repetitions, {el:.1f} s, fp64 C, 1 thread"}
+
+
+def _cpu_sample_all_cores(batch, target_s=10.0):
+    """The same oracle on every host core: one thread per core, each verifying
+    the same 16 requests repeatedly for ~target_s (the C oracle keeps no shared
+    state, and ctypes releases the GIL during the call)."""
+    import concurrent.futures as cf
+    import oracle
+    n_req = 16
+    rows = n_req * (batch.K + 1)
+    z, q = batch.logits[:rows], batch.q[: n_req * batch.K]
+    x, u = batch.draft[: n_req * batch.K], batch.uniforms[:rows]
+    cores = os.cpu_count() or 1
+    oracle.verify_fixed(z, q, x, u, n_req, batch.K, batch.temperature)  # builds and loads the library once
+    t0 = time.perf_counter()
+    deadline = t0 + target_s
+
+    def work():
+        reps = 0
+        while time.perf_counter() < deadline:
+            oracle.verify_fixed(z, q, x, u, n_req, batch.K, batch.temperature)
+            reps += 1
+        return reps
+
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        reps = sum(f.result() for f in [ex.submit(work) for _ in range(cores)])
+    el = time.perf_counter() - t0
+    return {"value": reps * n_req * batch.K / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {n_req} of 64 requests on each of {cores} threads, {reps} verifications in "
+                      f"{el:.1f} s, fp64 C"}
 
 
 def run_reference(args):
@@ -251,16 +297,13 @@ def run_ours(args):
     else:
         ms = ev[0][0].elapsed_time(ev[0][1]) / args.steps
     kms = ms * args.steps / launches  # one kernel per step: its mean duration, launch gap included
-    if world > 1:
-        t = torch.tensor([ms, kms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, kms = t.tolist()
+    ms, kms = _max_over_ranks([ms, kms], dev)
 
     # outcome of the step (same every step: same inputs)
     al_h = al.cpu()
     n_reject = int((al_h <= K).sum())
     units = Bn * K
-    value = world * units / (ms * 1e-3)
+    value = _job_value(world, units, ms)
     nominal = W.nominal_bytes(batch)
     logits_bytes = R * V * 4
     gathers = Bn * K * 16 + R * 4 + Bn * 4
@@ -300,12 +343,10 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / n_e2e
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = t.item()
+    e2e_ms = _max_over_ranks([e2e_ms], dev)[0]
 
     cpu = _cpu_sample(batch) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    cpu_all = _cpu_sample_all_cores(batch) if (rank == 0 and world == 1 and not args.no_cpu) else None
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -326,7 +367,8 @@ def run_ours(args):
                      "frac": achieved / peak, "traffic": _traffic("fused_kernel"),
                      "algorithmic_bytes_per_launch": kernel_alg, "ms_per_launch": kms},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * units / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "cpu_baseline_all_cores": cpu_all,
+        "e2e": {"value": _job_value(world, units, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "clocks": clk,
         "gpu_launches": launches,
