@@ -74,6 +74,7 @@ struct Args {
     int n_pe;            // partial records per row
     int n_seg;           // 256-token segments per row
     int n_rb;            // residual blocks per row
+    int keep_rows;       // fused kernel: leading rows per request kept in L2 for the residual pass
 };
 
 constexpr long long kWaitBudget = 4000000000ll;  // SM cycles (~2 s) before a wait gives up
@@ -1267,6 +1268,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
             };
             bool ok = true;
             const uint32_t total_rb = kSample ? static_cast<uint32_t>(a.B) * static_cast<uint32_t>(a.n_rb) : 0u;
+            // L2 priorities: a request's first rows are the ones its residual pass most often re-reads
+            // (acceptance decays with position, so the earliest drafts are the likeliest to be rejected):
+            // its first keep_rows rows stay (evict_last), sized on the host to half of L2; every other
+            // stats row and every residual read goes first.
+            const uint64_t keep = l2_evict_last_policy(), stream_through = l2_evict_first_policy();
             int jn = static_cast<int>(atomicAdd(a.sched + 0, 1u));
             uint32_t pn = 0xffffffffu;     // next residual claim (in flight)
             int nb_req = -1;               // request of the next claim whose decision words were read ahead
@@ -1279,6 +1285,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                     const int j = jn;
                     jn = static_cast<int>(atomicAdd(a.sched + 0, 1u));  // in flight while this block is issued
                     const int row = j / nb;
+                    const bool first_row = kSample && (a.row_offsets ? row - __ldg(a.row_offsets + request_of_row(a, row)) < a.keep_rows
+                                                                     : row % (a.K + 1) < a.keep_rows);
                     const int first = (j - row * nb) * kBlockChunks;
                     const int cnt = min(kBlockChunks, a.n_chunks - first);
                     for (int cc = 0; cc < cnt; ++cc) {
@@ -1293,8 +1301,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                         sm.tag[s] = Tag{kStats, row, chunk, n, 0, cc == cnt - 1 ? 1 : 0, 0.f, 0.f};
                         const uint32_t bytes = static_cast<uint32_t>(n) * sizeof(T);
                         mbar_arrive_expect_tx(&sm.full[s], bytes);
-                        bulk_g2s(sm.ring[s], reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(row) * a.V + c0,
-                                 bytes, &sm.full[s]);
+                        bulk_g2s_hint(sm.ring[s],
+                                      reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(row) * a.V + c0, bytes,
+                                      &sm.full[s], first_row ? keep : stream_through);
                         ++k;
                     }
                     continue;
@@ -1348,10 +1357,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                     const uint32_t zb = static_cast<uint32_t>(n) * sizeof(T);
                     const uint32_t qb = has_q ? static_cast<uint32_t>(n) * 4u : 0u;
                     mbar_arrive_expect_tx(&sm.full[s], zb + qb);
-                    bulk_g2s(sm.ring[s], reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(crow) * a.V + c0, zb,
-                             &sm.full[s]);
+                    bulk_g2s_hint(sm.ring[s], reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(crow) * a.V + c0,
+                                  zb, &sm.full[s], stream_through);
                     if (has_q)
-                        bulk_g2s(sm.ring[s] + kResQOffset, a.q + static_cast<size_t>(cqrow) * a.V + c0, qb, &sm.full[s]);
+                        bulk_g2s_hint(sm.ring[s] + kResQOffset, a.q + static_cast<size_t>(cqrow) * a.V + c0, qb,
+                                      &sm.full[s], stream_through);
                     ++k;
                     if (st == 0 && pn < total_rb) {  // the next claim's decision, read ahead
                         nb_req = static_cast<int>(pn / static_cast<uint32_t>(a.n_rb));
@@ -1805,6 +1815,7 @@ static inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t
 // call whose counters or records exceed the capacities clears them first.
 constexpr int kTicketCap = 16384;
 constexpr int kSchedWords = 8;
+constexpr size_t kL2KeepBytes = 64ull << 20;  // fused kernel: logits rows kept in L2 (half of it)
 constexpr size_t kRecPartCap = 32768;  // fused partial records (rows x n_pe)
 constexpr size_t kRecMassCap = 65536;  // fused segment masses (B x n_seg)
 constexpr size_t kRecDecCap = 8192;    // fused decision words (2 B)
@@ -1979,6 +1990,12 @@ static sv_status run_typed(Args &a, bool sample, bool vec, int small_nr, cudaStr
     a.n_chunks = (a.V + chunk_elems<T>() - 1) / chunk_elems<T>();
     int launches = 0;
     a.n_pe = ((a.n_chunks + fz::kBlockChunks - 1) / fz::kBlockChunks) * fz::kCons;
+    {
+        // positions per request whose logits rows fit in half of L2 across the batch
+        const size_t per_position = static_cast<size_t>(a.B) * a.V * sizeof(T);
+        const size_t keep = per_position ? (kL2KeepBytes / per_position) : 0;
+        a.keep_rows = static_cast<int>(keep < static_cast<size_t>(kMaxRowsPerRequest) ? keep : kMaxRowsPerRequest);
+    }
     if (a.B > kTicketCap &&
         cudaMemsetAsync(a.tickets1, 0, sizeof(uint32_t) * (static_cast<size_t>(a.B) + kSchedWords), s) !=
             cudaSuccess)
