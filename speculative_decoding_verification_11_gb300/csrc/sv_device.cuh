@@ -189,6 +189,12 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return p;
 }
 
+__device__ __forceinline__ uint64_t l2_evict_normal_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 __device__ __forceinline__ uint64_t l2_evict_last_policy() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));

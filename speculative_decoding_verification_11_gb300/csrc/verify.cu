@@ -1270,9 +1270,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
             const uint32_t total_rb = kSample ? static_cast<uint32_t>(a.B) * static_cast<uint32_t>(a.n_rb) : 0u;
             // L2 priorities: a request's first rows are the ones its residual pass most often re-reads
             // (acceptance decays with position, so the earliest drafts are the likeliest to be rejected):
-            // its first keep_rows rows stay (evict_last), sized on the host to half of L2; every other
-            // stats row and every residual read goes first.
-            const uint64_t keep = l2_evict_last_policy(), stream_through = l2_evict_first_policy();
+            // its first keep_rows rows are loaded at normal priority (keep_rows sized on the host to a
+            // quarter of L2), every other stats row and every residual read as evict_first, so the kept
+            // rows outlive the stream without outliving the step's successors.
+            const uint64_t keep = l2_evict_normal_policy(), stream_through = l2_evict_first_policy();
             int jn = static_cast<int>(atomicAdd(a.sched + 0, 1u));
             uint32_t pn = 0xffffffffu;     // next residual claim (in flight)
             int nb_req = -1;               // request of the next claim whose decision words were read ahead
@@ -1815,7 +1816,7 @@ static inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t
 // call whose counters or records exceed the capacities clears them first.
 constexpr int kTicketCap = 16384;
 constexpr int kSchedWords = 8;
-constexpr size_t kL2KeepBytes = 64ull << 20;  // fused kernel: logits rows kept in L2 (half of it)
+constexpr size_t kL2KeepBytes = 32ull << 20;  // fused kernel: logits rows kept in L2 (a quarter of it)
 constexpr size_t kRecPartCap = 32768;  // fused partial records (rows x n_pe)
 constexpr size_t kRecMassCap = 65536;  // fused segment masses (B x n_seg)
 constexpr size_t kRecDecCap = 8192;    // fused decision words (2 B)
@@ -1991,7 +1992,7 @@ static sv_status run_typed(Args &a, bool sample, bool vec, int small_nr, cudaStr
     int launches = 0;
     a.n_pe = ((a.n_chunks + fz::kBlockChunks - 1) / fz::kBlockChunks) * fz::kCons;
     {
-        // positions per request whose logits rows fit in half of L2 across the batch
+        // positions per request whose logits rows fit in a quarter of L2 across the batch
         const size_t per_position = static_cast<size_t>(a.B) * a.V * sizeof(T);
         const size_t keep = per_position ? (kL2KeepBytes / per_position) : 0;
         a.keep_rows = static_cast<int>(keep < static_cast<size_t>(kMaxRowsPerRequest) ? keep : kMaxRowsPerRequest);
