@@ -1385,6 +1385,25 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                     mbar_wait_bounded(&sm.full[kk % kStages], (kk / kStages) & 1, kWaitBudget);
             }
         }
+        // This CTA streams nothing more.  The last producer out resets the scheduling counters
+        // and zeroes the decision records for the next call: every producer has read them by then
+        // (each request's decision is read before any of its residual blocks streams), and the
+        // counters are used by producers only.  Off the path of the final draws.
+        int last = 0;
+        if (lane == 0) {
+            __threadfence();
+            last = (atomicAdd(a.sched + 1, 1u) + 1u == gridDim.x) ? 1 : 0;
+            if (last) __threadfence();
+        }
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+            if (kSample)
+                for (int i = lane; i < 2 * a.B; i += 32) a.fdec[i] = 0ull;
+            if (lane == 0) {
+                a.sched[0] = 0u;
+                a.sched[2] = 0u;
+                a.sched[1] = 0u;
+            }
+        }
     } else if (warp == kWorker) {
         for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
             Sel sel;
@@ -1463,33 +1482,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                                    enc_partial<kSample>(wa, wb));
                 open = 0;
             }
-        }
-    }
-    // the last CTA out resets the counters (and, after a timeout, every record) for the next call
-    __shared__ int s_last;
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        const uint32_t done = atomicAdd(a.sched + 1, 1u);
-        s_last = (done + 1u == gridDim.x) ? 1 : 0;
-    }
-    __syncthreads();
-    if (s_last) {
-        __threadfence();
-        if (kSample)
-            for (int i = tid; i < 2 * a.B; i += kThreads) a.fdec[i] = 0ull;
-        if (*reinterpret_cast<volatile uint32_t *>(a.status) & SV_FLAG_TIMEOUT) {
-            const size_t np = static_cast<size_t>(a.rows) * a.n_pe;
-            for (size_t i = tid; i < np; i += kThreads) a.fpart[i] = 0ull;
-            if (kSample) {
-                const size_t nm = static_cast<size_t>(a.B) * a.n_seg;
-                for (size_t i = tid; i < nm; i += kThreads) a.fmass[i] = 0u;
-            }
-        }
-        if (tid == 0) {
-            a.sched[0] = 0u;
-            a.sched[1] = 0u;
-            a.sched[2] = 0u;
         }
     }
 }
