@@ -75,6 +75,8 @@ struct Args {
     int n_seg;           // 256-token segments per row
     int n_rb;            // residual blocks per row
     int keep_rows;       // fused kernel: leading rows per request kept in L2 for the residual pass
+    int n_st;            // fused kernel: residual stages per row
+    int tail_b0;         // fused kernel: requests from here on take one-stage residual claims
 };
 
 constexpr long long kWaitBudget = 4000000000ll;  // SM cycles (~2 s) before a wait gives up
@@ -830,6 +832,27 @@ __device__ __forceinline__ void st_relaxed_u32(uint32_t *p, uint32_t v) {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Residual claims, in request order: a request before tail_b0 takes n_rb
+// claims of kResBlockStages stages; the last requests (decided last, since
+// stats stream in row order) take one claim per stage, so that their
+// residual spreads over many CTAs at the end of the step.
+struct Claim {
+    int b, st0, nst;
+};
+__device__ __forceinline__ uint32_t residual_claims(const Args &a) {
+    return static_cast<uint32_t>(a.tail_b0) * a.n_rb + static_cast<uint32_t>(a.B - a.tail_b0) * a.n_st;
+}
+__device__ __forceinline__ Claim decode_claim(uint32_t p, const Args &a) {
+    const uint32_t big = static_cast<uint32_t>(a.tail_b0) * a.n_rb;
+    if (p < big) {
+        const int b = static_cast<int>(p / static_cast<uint32_t>(a.n_rb));
+        return Claim{b, static_cast<int>(p - static_cast<uint32_t>(b) * a.n_rb) * kResBlockStages, kResBlockStages};
+    }
+    const uint32_t q = p - big;
+    const int i = static_cast<int>(q / static_cast<uint32_t>(a.n_st));
+    return Claim{a.tail_b0 + i, static_cast<int>(q - static_cast<uint32_t>(i) * a.n_st), 1};
+}
+
 // A partial (a, b) as one word: low half a; high half b with its top bit
 // flipped.  b is a sum of exponentials (>= +0) or a token index (>= 0), so
 // the high half is never zero.
@@ -1267,7 +1290,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                 return !*abort_flag;
             };
             bool ok = true;
-            const uint32_t total_rb = kSample ? static_cast<uint32_t>(a.B) * static_cast<uint32_t>(a.n_rb) : 0u;
+            const uint32_t total_rb = kSample ? residual_claims(a) : 0u;
             // L2 priorities: a request's first rows are the ones its residual pass most often re-reads
             // (acceptance decays with position, so the earliest drafts are the likeliest to be rejected):
             // its first keep_rows rows are loaded at normal priority (keep_rows sized on the host to a
@@ -1310,14 +1333,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                     continue;
                 }
                 if (!kSample) break;
-                // 2. residual blocks (kResBlockStages consecutive stages of one request's selected
-                // row), claimed grid-wide in request-major order.  One claim is kept in flight and
-                // its decision words are loaded while the current block's stages are issued.
+                // 2. residual claims (consecutive stages of one request's selected row), grid-wide
+                // in request order.  One claim is kept in flight and its decision words are loaded
+                // while the current claim's stages are issued.
                 if (pn == 0xffffffffu) pn = atomicAdd(a.sched + 2, 1u);
                 const uint32_t p = pn;
                 if (p >= total_rb) break;
-                const int b = static_cast<int>(p / static_cast<uint32_t>(a.n_rb));
-                const int blk = static_cast<int>(p % static_cast<uint32_t>(a.n_rb));
+                const Claim cl = decode_claim(p, a);
+                const int b = cl.b;
                 if (b != cb) {
                     uint64_t w0 = (b == nb_req) ? nw0 : ld_relaxed_u64(a.fdec + 2 * b);
                     uint64_t w1 = (b == nb_req) ? nw1 : ld_relaxed_u64(a.fdec + 2 * b + 1);
@@ -1345,8 +1368,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                 pn = atomicAdd(a.sched + 2, 1u);  // the next claim
                 if (crow < 0) continue;           // invalid request: nothing to draw
                 const bool has_q = cqrow >= 0;
-                for (int st = 0; st < kResBlockStages; ++st) {
-                    const int c0 = blk * kResBlockElems + st * kResElems;
+                for (int st = 0; st < cl.nst; ++st) {
+                    const int c0 = (cl.st0 + st) * kResElems;
                     if (c0 >= a.V) break;
                     const int n = min(kResElems, a.V - c0);
                     int s;
@@ -1365,7 +1388,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                                       &sm.full[s], stream_through);
                     ++k;
                     if (st == 0 && pn < total_rb) {  // the next claim's decision, read ahead
-                        nb_req = static_cast<int>(pn / static_cast<uint32_t>(a.n_rb));
+                        nb_req = decode_claim(pn, a).b;
                         if (nb_req != cb) {
                             nw0 = ld_relaxed_u64(a.fdec + 2 * nb_req);
                             nw1 = ld_relaxed_u64(a.fdec + 2 * nb_req + 1);
@@ -1983,6 +2006,11 @@ static sv_status run_typed(Args &a, bool sample, bool vec, int small_nr, cudaStr
     a.n_chunks = (a.V + chunk_elems<T>() - 1) / chunk_elems<T>();
     int launches = 0;
     a.n_pe = ((a.n_chunks + fz::kBlockChunks - 1) / fz::kBlockChunks) * fz::kCons;
+    a.n_st = (a.V + kResStageElems - 1) / kResStageElems;
+    {
+        const int tail = a.B / 8 > 0 ? a.B / 8 : 1;  // the last eighth of the requests
+        a.tail_b0 = a.B - (tail < a.B ? tail : a.B);
+    }
     {
         // positions per request whose logits rows fit in a quarter of L2 across the batch
         const size_t per_position = static_cast<size_t>(a.B) * a.V * sizeof(T);
