@@ -361,7 +361,7 @@ static bool encode_bf16_kmajor(CUtensorMap *map, const void *base, int rows, int
 }
 
 struct LmLayout {
-    size_t finish, partials, spill, total;
+    size_t finish, partials, segs, spill, total;
 };
 
 static inline size_t a256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -394,6 +394,8 @@ static LmLayout lm_layout(int B, int K, int V) {
     o = a256(o + finish_workspace_size(B, M, V));
     L.partials = o;
     o = a256(o + sizeof(float2) * static_cast<size_t>(M) * n_tiles);
+    L.segs = o;  // per request, one sum per 256-token segment (the cluster finish's scratch)
+    o = a256(o + sizeof(float) * static_cast<size_t>(B) * ((V + kSegElems - 1) / kSegElems));
     L.spill = o;
     o = a256(o + sizeof(float) * static_cast<size_t>(M) * V);
     L.total = o;
@@ -602,6 +604,347 @@ __global__ void __launch_bounds__(kDraftThreads) draft_finish_kernel(float *q, c
     }
 }
 
+// ---------------------------------------------------------------------------
+// Verification after the LM-head GEMM, one cluster of kFinC CTAs per request.
+// The GEMM left the fp32 logits (the spill, mostly in L2) and one partial per
+// row and GEMM CTA.  Every CTA merges the request's row partials and runs the
+// accept tests and the first-reject scan (the same result in each; rank 0
+// writes it).  For the final draw each CTA computes r over its contiguous
+// slice of 256-token segments straight from L2 into registers, keeps the
+// segment sums in shared memory (and in a global scratch row), and sends its
+// slice total to every CTA of the cluster with remote stores.  After one
+// cluster barrier each CTA holds all slice totals, computes the same prefix,
+// R and u R, and the one CTA whose slice holds u R finds the segment in its
+// own shared memory and the token in that segment (double-single prefix,
+// in-segment running sums, the usual rounding fallbacks).  Nothing reads
+// another CTA's shared memory after the barrier, so no CTA waits for another
+// to finish.
+// ---------------------------------------------------------------------------
+constexpr int kFinC = 8;            // CTAs per request
+constexpr int kFinThreads = 512;
+constexpr int kFinWarps = kFinThreads / 32;
+constexpr int kFinBatch = 2;        // segments whose loads a warp holds in flight at once
+constexpr int kFinMaxSegs = 96;     // segments per CTA: V <= kFinC x 96 x 256 = 196608
+
+__host__ __device__ constexpr int fin_segs_per_cta(int V) {
+    return ((V + kSegElems - 1) / kSegElems + kFinC - 1) / kFinC;
+}
+
+// The 8 tokens a lane holds in 256-token segment g: token g * 256 + (j * 32 +
+// lane) * 4 + k, j < 2, k < 4 (zero beyond V).  Loading and computing are
+// split so that a warp can hold several segments' loads in flight.
+__device__ __forceinline__ void fin_fetch(const float *zrow, const float *qrow, int V, int g, int lane,
+                                          float4 (&z)[2], float4 (&qv)[2]) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int e0 = g * kSegElems + (j * 32 + lane) * 4;
+        const bool in = e0 < V;
+        z[j] = in ? __ldcs(reinterpret_cast<const float4 *>(zrow + e0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        qv[j] = (in && qrow) ? __ldcs(reinterpret_cast<const float4 *>(qrow + e0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+// r(v) = max(0, p(v) - q(v)) of those tokens (p(v) alone without a q row),
+// p(v) = 2^(z(v) c - M) / S.
+__device__ __forceinline__ void fin_r(const float4 (&z)[2], const float4 (&qv)[2], bool has_q, int V, int g,
+                                      int lane, float c, float M, float invS, float (&r)[2][4]) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const bool in = g * kSegElems + (j * 32 + lane) * 4 < V;
+        const float zz[4] = {z[j].x, z[j].y, z[j].z, z[j].w}, qq[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float p = __fmul_rn(ex2(__fmaf_rn(zz[k], c, -M)), invS);
+            r[j][k] = in ? (has_q ? fmaxf(__fsub_rn(p, qq[k]), 0.f) : p) : 0.f;
+        }
+    }
+}
+__device__ __forceinline__ void fin_load_r(const float *zrow, const float *qrow, int V, int g, int lane, float c,
+                                           float M, float invS, float (&r)[2][4]) {
+    float4 z[2], qv[2];
+    fin_fetch(zrow, qrow, V, g, lane, z, qv);
+    fin_r(z, qv, qrow != nullptr, V, g, lane, c, M, invS, r);
+}
+
+// Sum of segment g's r over the whole row: this CTA's own segments from
+// shared memory, the others from the global scratch row (written before the
+// cluster barrier by the CTA that owns them).
+__device__ __forceinline__ float fin_seg_mass(const float *s_seg, const float *gseg, int g, int seg0, int seg1) {
+    return (g >= seg0 && g < seg1) ? s_seg[g - seg0] : __ldcg(gseg + g);
+}
+
+// First token with r > 0 at or after segment g0 (forward) or the last one at
+// or before it (backward); -1 if there is none.  Warp-wide; 32 segment sums
+// are examined per step.
+template <bool kForward>
+__device__ int fin_find_positive(const float *zrow, const float *qrow, int V, int ns, float c, float M, float invS,
+                                 const float *s_seg, const float *gseg, int seg0, int seg1, int g0, int lane,
+                                 float *rv) {
+    for (int base = g0; kForward ? base < ns : base >= 0; base += kForward ? 32 : -32) {
+        const int g = kForward ? base + lane : base - lane;
+        const bool has = (kForward ? g < ns : g >= 0) && fin_seg_mass(s_seg, gseg, g, seg0, seg1) > 0.f;
+        const unsigned m = __ballot_sync(0xffffffffu, has);
+        if (!m) continue;
+        const int gs = __shfl_sync(0xffffffffu, g, __ffs(m) - 1);
+        float r[2][4];
+        fin_load_r(zrow, qrow, V, gs, lane, c, M, invS, r);
+        int loc = kForward ? 0x7fffffff : -1;
+        float rloc = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int jj = kForward ? 1 - j : j, kk = kForward ? 3 - k : k;  // keep the extreme one
+                if (r[jj][kk] > 0.f) {
+                    loc = (jj * 32 + lane) * 4 + kk;
+                    rloc = r[jj][kk];
+                }
+            }
+        const int best = kForward ? __reduce_min_sync(0xffffffffu, loc) : __reduce_max_sync(0xffffffffu, loc);
+        if (kForward ? best == 0x7fffffff : best < 0) continue;  // a positive sum of nothing: cannot happen
+        const unsigned mm = __ballot_sync(0xffffffffu, loc == best);
+        *rv = __shfl_sync(0xffffffffu, rloc, __ffs(mm) - 1);
+        return gs * kSegElems + best;
+    }
+    return -1;
+}
+
+template <bool kSample>
+__global__ void __launch_bounds__(kFinThreads, 2) verify_finish_kernel(const float *spill, const float2 *partials,
+                                                                    int n_parts, const float *q, int K, int V,
+                                                                    float c, const int32_t *draft,
+                                                                    const float *uniforms, int32_t *out_tokens,
+                                                                    int32_t *accept_len, float *diag,
+                                                                    uint32_t *status, float *seg_scratch, int B) {
+    pdl_wait_prior_grid();  // the spill and the partials come from the GEMM before it
+    pdl_launch_dependents();
+    const uint32_t rank = cluster_ctarank();
+    const int b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nr = K + 1, r0 = b * nr, d0 = b * K, n_draft = B * K;
+    const int nsp = fin_segs_per_cta(V), ns = (V + kSegElems - 1) / kSegElems;
+    const int seg0 = min(static_cast<int>(rank) * nsp, ns), seg1 = min(seg0 + nsp, ns), nloc = seg1 - seg0;
+    __shared__ float2 s_row[SV_MAX_K + 1];
+    __shared__ int s_x[SV_MAX_K];
+    __shared__ float s_z[SV_MAX_K], s_q[SV_MAX_K], s_u[SV_MAX_K];
+    __shared__ float s_seg[kFinMaxSegs];
+    __shared__ float2 s_tot[2][kFinC];  // slice totals (double-single), written by every CTA of the cluster
+    __shared__ int s_ks, s_retry;
+
+    // accept-test operands of draft j = tid: independent of the merge below, so issued first
+    int xj = -1;
+    float zj = 0.f, qj = 0.f, uj = 0.f;
+    if (tid < K) {
+        xj = __ldg(draft + d0 + tid);
+        if (xj < 0 || xj >= V) {
+            xj = -1;
+        } else if (kSample) {
+            zj = __ldcg(spill + static_cast<size_t>(r0 + tid) * V + xj);
+            qj = __ldg(q + static_cast<size_t>(d0 + tid) * V + xj);
+            uj = __ldg(uniforms + r0 + tid);
+        }
+    }
+    // row normalisers: warp w merges rows w, w + 16, ... over the GEMM's CTAs, in order
+    for (int j = warp; j < nr; j += kFinWarps) {
+        float ra;
+        int rb;
+        partial_identity<kSample>(ra, rb);
+        for (int i = lane; i < n_parts; i += 32)
+            merge_pair<kSample>(ra, rb, partials[static_cast<size_t>(r0 + j) * n_parts + i]);
+        warp_partial_reduce<kSample>(ra, rb);
+        if (lane == 0) s_row[j] = make_float2(ra, __int_as_float(rb));
+    }
+    if (tid < K) {
+        s_x[tid] = xj;
+        s_z[tid] = zj;
+        s_q[tid] = qj;
+        s_u[tid] = uj;
+    }
+    __syncthreads();
+
+    // accept tests and first-reject scan (warp 0 of every CTA; rank 0 writes the outputs)
+    if (warp == 0) {
+        bool bad = false;
+        for (int j = lane; j < K; j += 32) bad |= s_x[j] < 0;
+        bad = __any_sync(0xffffffffu, bad);
+        int ks = -1;
+        for (int jb = 0; !bad && jb < nr && ks < 0; jb += 32) {
+            const int j = jb + lane;
+            bool rej = false;
+            if (j < K) {
+                const float2 sj = s_row[j];
+                if (kSample) {
+                    const float p = exp2f(fmaf(s_z[j], c, -sj.x)) / sj.y;
+                    rej = !(s_u[j] * s_q[j] <= p);
+                    if (diag && rank == 0) diag[d0 + j] = p;
+                } else {
+                    rej = (s_x[j] != __float_as_int(sj.y));
+                }
+            }
+            const unsigned m = __ballot_sync(0xffffffffu, rej);
+            if (m) ks = jb + __ffs(m) - 1;
+            else if (jb + 32 >= nr) ks = K;
+        }
+        if (rank == 0) {
+            if (bad) {
+                for (int j = lane; j < nr; j += 32) out_tokens[r0 + j] = -1;
+                if (lane == 0) {
+                    accept_len[b] = 0;
+                    atomicOr(status, SV_FLAG_BAD_TOKEN);
+                }
+            } else {
+                for (int j = lane; j < nr; j += 32) {
+                    int v = -1;
+                    if (j < ks) v = s_x[j];
+                    else if (j == ks && !kSample) v = __float_as_int(s_row[ks].y);
+                    out_tokens[r0 + j] = v;
+                }
+                if (lane == 0) accept_len[b] = ks + 1;
+            }
+        }
+        if (lane == 0) s_ks = bad ? -1 : ks;
+    }
+    __syncthreads();
+    // every CTA of the cluster has the same ks: leaving together touches no other CTA's memory
+    if (!kSample || s_ks < 0) return;
+
+    const int ks = s_ks;
+    const float M = s_row[ks].x, invS = 1.f / s_row[ks].y;
+    const float *zrow = spill + static_cast<size_t>(r0 + ks) * V;
+    const float *qrow0 = (ks < K) ? q + static_cast<size_t>(d0 + ks) * V : nullptr;
+    float *gseg = seg_scratch + static_cast<size_t>(b) * ns;
+    // warp 0's share of the local segments and its exclusive prefix within the slice
+    const int G = (nloc + 31) / 32;
+    const int i0 = min(lane * G, nloc), i1 = min(i0 + G, nloc);
+    DS excl{0.f, 0.f};
+    int attempt = 0;
+    const float *qrow = qrow0;
+    for (;; ++attempt) {
+        qrow = (attempt == 0) ? qrow0 : nullptr;
+        // r over this CTA's segments, kFinBatch segments per warp in flight
+        for (int gb = seg0 + warp; gb < seg1; gb += kFinBatch * kFinWarps) {
+            float4 zb[kFinBatch][2], qb[kFinBatch][2];
+#pragma unroll
+            for (int i = 0; i < kFinBatch; ++i) {
+                const int g = gb + i * kFinWarps;
+                if (g < seg1) fin_fetch(zrow, qrow, V, g, lane, zb[i], qb[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < kFinBatch; ++i) {
+                const int g = gb + i * kFinWarps;
+                if (g < seg1) {
+                    float r[2][4];
+                    fin_r(zb[i], qb[i], qrow != nullptr, V, g, lane, c, M, invS, r);
+                    const float s = seg_sum(r);
+                    if (lane == 0) {
+                        s_seg[g - seg0] = s;
+                        gseg[g] = s;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        // the slice total, in a fixed order, to every CTA of the cluster
+        if (warp == 0) {
+            DS sum{0.f, 0.f};
+            for (int i = i0; i < i1; ++i) sum = ds_add_f(sum, s_seg[i]);
+            DS incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const DS y = ds_shfl_up(incl, o);
+                if (lane >= o) incl = ds_add(incl, y);
+            }
+            excl = ds_shfl_up(incl, 1);
+            if (lane == 0) excl = DS{0.f, 0.f};
+            const DS tot = ds_shfl(incl, 31);
+            if (lane < kFinC) st_dsmem_f32x2(&s_tot[attempt][rank], tot.hi, tot.lo, static_cast<uint32_t>(lane));
+        }
+        cluster_sync();
+        // the same totals in the same order in every CTA: an empty residual is seen by all of them
+        if (attempt == 0 && qrow0 != nullptr) {
+            if (tid == 0) {
+                DS R{0.f, 0.f};
+                for (int k = 0; k < kFinC; ++k) R = ds_add(R, DS{s_tot[0][k].x, s_tot[0][k].y});
+                s_retry = R.hi > 0.f ? 0 : 1;
+            }
+            __syncthreads();
+            if (s_retry) {
+                if (rank == 0 && tid == 0) atomicOr(status, SV_FLAG_ZERO_RESIDUAL);  // draw from p
+                continue;
+            }
+        }
+        break;
+    }
+    if (warp != 0) return;
+
+    // prefix of the slice totals, R, u R and the CTA whose slice holds u R
+    const float u = __ldg(uniforms + r0 + K);
+    DS P{0.f, 0.f}, Pmine{0.f, 0.f};
+    DS Pk[kFinC + 1];
+    Pk[0] = P;
+#pragma unroll
+    for (int k = 0; k < kFinC; ++k) {
+        P = ds_add(P, DS{s_tot[attempt][k].x, s_tot[attempt][k].y});
+        Pk[k + 1] = P;
+    }
+    const DS R = P;
+    const DS t = ds_mul_f(R, u);
+    int owner = -1, last_pos = -1;
+#pragma unroll
+    for (int k = kFinC - 1; k >= 0; --k) {
+        if (ds_gt(Pk[k + 1], t)) owner = k;
+        if (last_pos < 0 && s_tot[attempt][k].x > 0.f) last_pos = k;
+    }
+#pragma unroll
+    for (int k = 0; k < kFinC; ++k)
+        if (k == static_cast<int>(rank)) Pmine = Pk[k];
+    const bool past_end = owner < 0;  // u R at or above every boundary: the last r > 0
+    if (past_end) owner = last_pos < 0 ? 0 : last_pos;
+    if (owner != static_cast<int>(rank)) return;
+
+    int vstar = -1;
+    float rstar = 0.f;
+    if (!past_end) {
+        // the first local segment whose running sum passes u R
+        DS Pl = ds_add(Pmine, excl);
+        int found = -1;
+        DS fb{0.f, 0.f};
+        for (int i = i0; i < i1; ++i) {
+            const DS Pn = ds_add_f(Pl, s_seg[i]);
+            if (found < 0 && ds_gt(Pn, t)) {
+                found = i;
+                fb = Pl;
+            }
+            Pl = Pn;
+        }
+        const unsigned ball = __ballot_sync(0xffffffffu, found >= 0);
+        int next = seg1;  // sums short of u R: the next r > 0 after the slice
+        if (ball) {
+            const int src = __ffs(ball) - 1;
+            const int fseg = seg0 + __shfl_sync(0xffffffffu, found, src);
+            const DS fbase = ds_shfl(fb, src);
+            float r[2][4];
+            fin_load_r(zrow, qrow, V, fseg, lane, c, M, invS, r);
+            const TileScan ts = warp_seg_scan(r, fseg, V, fbase, t, lane);
+            vstar = ts.v;
+            rstar = ts.rv;
+            next = fseg + 1;
+        }
+        if (vstar < 0)
+            vstar = fin_find_positive<true>(zrow, qrow, V, ns, c, M, invS, s_seg, gseg, seg0, seg1, next, lane,
+                                            &rstar);
+    }
+    if (vstar < 0)
+        vstar = fin_find_positive<false>(zrow, qrow, V, ns, c, M, invS, s_seg, gseg, seg0, seg1, ns - 1, lane,
+                                         &rstar);
+    if (lane == 0) {
+        out_tokens[r0 + ks] = vstar;
+        if (diag) {
+            const float Rf = __fadd_rn(R.hi, R.lo);
+            diag[n_draft + 2 * b] = Rf;
+            diag[n_draft + 2 * b + 1] = __fdiv_rn(rstar, Rf);
+        }
+    }
+}
+
 }  // namespace lm
 }  // namespace sv
 
@@ -657,6 +1000,34 @@ extern "C" sv_status spec_lmhead_verify(const void *hidden, const void *w_vocab_
     else lm::launch_gemm_bn<false>(bn, ta, tb, a, grid, s);
     prof_end(s);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    if (V % 4 == 0 && lm::fin_segs_per_cta(V) <= lm::kFinMaxSegs &&
+        (!sample || K == 0 || (reinterpret_cast<uintptr_t>(q) & 15u) == 0)) {
+        // one cluster of kFinC CTAs per request over the spill and the partials
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(lm::kFinC, B);
+        cfg.blockDim = dim3(lm::kFinThreads);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = lm::kFinC;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        const float *spill = reinterpret_cast<const float *>(w + L.spill);
+        const float2 *parts = a.partials;
+        float *segs = reinterpret_cast<float *>(w + L.segs);
+        const cudaError_t e =
+            sample ? cudaLaunchKernelEx(&cfg, lm::verify_finish_kernel<true>, spill, parts, grid, q, K, V, a.c, draft,
+                                        uniforms, out_tokens, accept_len, diag, a.status, segs, B)
+                   : cudaLaunchKernelEx(&cfg, lm::verify_finish_kernel<false>, spill, parts, grid, q, K, V, a.c, draft,
+                                        uniforms, out_tokens, accept_len, static_cast<float *>(nullptr), a.status,
+                                        segs, B);
+        set_launches(2);
+        return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+    }
     int more = 0;
     const sv_status st = finish_from_partials(reinterpret_cast<const float *>(w + L.spill), a.partials, grid, q,
                                               B, K, V, sample ? temperature : 1.f, sample, draft, uniforms,

@@ -245,6 +245,15 @@ __device__ __forceinline__ float ld_dsmem_f32(const float *p, uint32_t rank) {
     return v;
 }
 
+// Store two floats into the shared memory of CTA `rank` of this cluster, at
+// the address that `p` has in this CTA (8-byte aligned).  Visible to that CTA
+// after the next cluster barrier.
+__device__ __forceinline__ void st_dsmem_f32x2(float2 *p, float a, float b, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(p)), "r"(rank));
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(a), "f"(b) : "memory");
+}
+
 }  // namespace sv
 
 namespace sv {
