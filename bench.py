@@ -42,25 +42,31 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def _source_hash():
+# the sources each profiled kernel is built from (its own file and the shared device headers)
+KERNEL_SOURCES = {
+    "fused_kernel": ("verify.cu", "sv_device.cuh", "sv_draw.cuh", "sv_host.h"),
+    "lmhead_gemm_kernel": ("lmhead.cu", "sv_device.cuh", "sv_draw.cuh", "sv_host.h"),
+}
+
+
+def _source_hash(kernel: str):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_11_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in sorted(KERNEL_SOURCES[kernel]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def _traffic(kernel: str):
     """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the kernel's current sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         rec = d.get(kernel)
-        if rec and rec.get("source_hash") == _source_hash():
+        if rec and rec.get("source_hash") == _source_hash(kernel):
             return rec["dram_bytes_per_launch"]
     except Exception:
         pass
