@@ -236,7 +236,7 @@ def lmhead(seed: int = 1003, B: int = 16, K: int = 7, d: int = 8192, V: int = 12
     draft_logits = torch.cat(qs, dim=1)
     q = _softmax_rows_f32(draft_logits, T)
     del draft_logits
-    x = _draw_from(q, g)
+    x = _draw_from(q, g) if q.shape[0] else torch.empty(0, dtype=torch.int32)
     u = torch.from_numpy(philox_uniforms(seed, R, stream=0))
     return Batch(name="lmhead", logits=None, q=q, draft=x, uniforms=u,
                  row_offsets=row_offsets, B=B, K=K, V=V, temperature=T,

@@ -12,6 +12,8 @@ rule is the verifier's with its bands widened to cover that error:
 """
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -101,6 +103,55 @@ def test_lmhead_m128_greedy(cuda_device, m128_batch):
 def test_lmhead_full_workload(cuda_device):
     b = W.lmhead()
     _compare("lmhead B=16 K=7 d=8192 V=128256 T=1", b, 1.0, cuda_device)
+
+
+def _lm_status(dev):
+    ws = api._default_ws[(str(dev), torch.cuda.current_stream(dev).cuda_stream)].buf
+    return B_.spec_verify_last_device_status(ws)
+
+
+def test_lmhead_k_zero_is_bonus_only(cuda_device):
+    """Plain decoding through the same call: one row per request, the token
+    drawn from p."""
+    b = W.lmhead(seed=3311, B=12, K=0, d=512, V=6000, d_draft=256)
+    _compare("lmhead K=0 B=12 d=512 V=6000 T=1", b, 1.0, cuda_device)
+
+
+def test_lmhead_vocab_not_multiple_of_4(cuda_device):
+    """Element-wise logits copy in the GEMM epilogue and the two-kernel finish."""
+    b = W.lmhead(seed=3313, B=5, K=3, d=512, V=4001, d_draft=256, T=0.9)
+    _compare("lmhead B=5 K=3 d=512 V=4001 T=0.9", b, 0.9, cuda_device)
+
+
+def test_lmhead_zero_residual_falls_back_to_p(cuda_device):
+    """q >= p everywhere: every residual is empty, so the token is drawn from
+    p and the call flags it."""
+    b = W.lmhead(seed=3312, B=6, K=3, d=512, V=8192, d_draft=256)
+    b = dataclasses.replace(b, q=torch.ones_like(b.q))
+    _lm_status(cuda_device)  # clears the status word
+    _compare("lmhead zero residual B=6 K=3 d=512 V=8192", b, 1.0, cuda_device)
+    st, flags = _lm_status(cuda_device)
+    assert st == B_.SV_OK and flags & B_.SV_FLAG_ZERO_RESIDUAL
+
+
+def test_lmhead_residual_at_one_token_forces_it(cuda_device):
+    """q = 1 except q(t) = 0 for one token t per request: the draft is
+    rejected (u q(x) > p(x)) and r > 0 at t alone, so the token drawn is t
+    whatever u is.  The targets sit in different slices of the finish
+    cluster, on both sides of a slice boundary and in the ragged last
+    segment."""
+    V = 20000
+    targets = [5, 2559, 2560, 7777, 12345, 17999, 19968, 19999]
+    b = W.lmhead(seed=3314, B=len(targets), K=1, d=512, V=V, d_draft=256)
+    q = torch.ones_like(b.q)
+    for i, t in enumerate(targets):
+        q[i, t] = 0.0
+    b = dataclasses.replace(b, q=q)
+    out, al, _ = _run(b, cuda_device, 1.0)
+    for i, t in enumerate(targets):
+        if int(b.draft[i]) != t:
+            assert al[i] == 1 and out[2 * i] == t, (i, t, al[i], out[2 * i])
+    _compare("lmhead one-token residual B=8 K=1 d=512 V=20000", b, 1.0, cuda_device)
 
 
 def test_lmhead_argument_errors(cuda_device):
