@@ -77,6 +77,7 @@ struct Args {
     int keep_rows;       // fused kernel: leading rows per request kept in L2 for the residual pass
     int n_st;            // fused kernel: residual stages per row
     int tail_b0;         // fused kernel: requests from here on take one-stage residual claims
+    int early_res;       // fused kernel: residual claims may start during the stats stream
 };
 
 constexpr long long kWaitBudget = 4000000000ll;  // SM cycles (~2 s) before a wait gives up
@@ -1303,9 +1304,65 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
             uint64_t nw0 = 0ull, nw1 = 0ull;
             int cb = -1, crow = -1, cqrow = -1;  // the last decision read
             float cM = 0.f, cinvS = 0.f;
+            // the stages of one residual claim (b's selected row and, after a rejection, its q row)
+            auto issue_claim = [&](const Claim &cl, int row, int qrow, float M, float invS) -> bool {
+                const bool has_q = qrow >= 0;
+                for (int st = 0; st < cl.nst; ++st) {
+                    const int c0 = (cl.st0 + st) * kResElems;
+                    if (c0 >= a.V) break;
+                    const int n = min(kResElems, a.V - c0);
+                    int s;
+                    if (!claim(s)) return false;
+                    sm.tag[s] = Tag{kRes, cl.b, c0 / kResElems, n, has_q ? 1 : 0, 0, M, invS};
+                    const uint32_t zb = static_cast<uint32_t>(n) * sizeof(T);
+                    const uint32_t qb = has_q ? static_cast<uint32_t>(n) * 4u : 0u;
+                    mbar_arrive_expect_tx(&sm.full[s], zb + qb);
+                    bulk_g2s_hint(sm.ring[s], reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(row) * a.V + c0,
+                                  zb, &sm.full[s], stream_through);
+                    if (has_q)
+                        bulk_g2s_hint(sm.ring[s] + kResQOffset, a.q + static_cast<size_t>(qrow) * a.V + c0, qb,
+                                      &sm.full[s], stream_through);
+                    ++k;
+                }
+                return true;
+            };
+            // With early_res, a producer holds at most one residual claim during the stats stream.
+            // Its request's decision words are loaded one stats block ahead; once they are out, the
+            // claim's stages go ahead of the next stats block, while the request's rows are still in
+            // L2.  Chosen on the host when no logits row can be kept in L2 through the whole stream:
+            // then the residual pass after the stream would re-read every selected row from DRAM.
+            uint32_t held = 0xffffffffu;
+            bool claims_left = kSample && a.early_res != 0;
+            uint64_t hw0 = 0ull, hw1 = 0ull;
             while (ok) {
                 // 1. stats blocks first (row order, grid-wide counter): the decisions wait on them
                 if (jn < total_blocks) {
+                    if (kSample && (claims_left || held != 0xffffffffu)) {
+                        if (held != 0xffffffffu && (hw0 >> 32) != 0 && (hw1 >> 32) != 0) {
+                            const int hrow = static_cast<int>(static_cast<uint32_t>(hw1));
+                            if (hrow >= 0 &&
+                                !issue_claim(decode_claim(held, a), hrow,
+                                             static_cast<int>(static_cast<uint32_t>(hw1 >> 32)) - 2,
+                                             __uint_as_float(static_cast<uint32_t>(hw0)),
+                                             __uint_as_float(static_cast<uint32_t>(hw0 >> 32) ^ 0x80000000u))) {
+                                ok = false;
+                                break;
+                            }
+                            held = 0xffffffffu;
+                        }
+                        if (held == 0xffffffffu && claims_left) {
+                            held = atomicAdd(a.sched + 2, 1u);
+                            if (held >= total_rb) {
+                                held = 0xffffffffu;
+                                claims_left = false;
+                            }
+                        }
+                        if (held != 0xffffffffu) {  // checked before the next stats block
+                            const int hb = decode_claim(held, a).b;
+                            hw0 = ld_relaxed_u64(a.fdec + 2 * hb);
+                            hw1 = ld_relaxed_u64(a.fdec + 2 * hb + 1);
+                        }
+                    }
                     const int j = jn;
                     jn = static_cast<int>(atomicAdd(a.sched + 0, 1u));  // in flight while this block is issued
                     const int row = j / nb;
@@ -1336,6 +1393,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                 // 2. residual claims (consecutive stages of one request's selected row), grid-wide
                 // in request order.  One claim is kept in flight and its decision words are loaded
                 // while the current claim's stages are issued.
+                if (held != 0xffffffffu) {  // the claim held through the stats stream comes first
+                    pn = held;
+                    nb_req = decode_claim(held, a).b;
+                    nw0 = hw0;
+                    nw1 = hw1;
+                    held = 0xffffffffu;
+                }
                 if (pn == 0xffffffffu) pn = atomicAdd(a.sched + 2, 1u);
                 const uint32_t p = pn;
                 if (p >= total_rb) break;
@@ -1366,37 +1430,17 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                     cinvS = __uint_as_float(static_cast<uint32_t>(w0 >> 32) ^ 0x80000000u);
                 }
                 pn = atomicAdd(a.sched + 2, 1u);  // the next claim
-                if (crow < 0) continue;           // invalid request: nothing to draw
-                const bool has_q = cqrow >= 0;
-                for (int st = 0; st < cl.nst; ++st) {
-                    const int c0 = (cl.st0 + st) * kResElems;
-                    if (c0 >= a.V) break;
-                    const int n = min(kResElems, a.V - c0);
-                    int s;
-                    if (!claim(s)) {
-                        ok = false;
-                        break;
-                    }
-                    sm.tag[s] = Tag{kRes, b, c0 / kResElems, n, has_q ? 1 : 0, 0, cM, cinvS};
-                    const uint32_t zb = static_cast<uint32_t>(n) * sizeof(T);
-                    const uint32_t qb = has_q ? static_cast<uint32_t>(n) * 4u : 0u;
-                    mbar_arrive_expect_tx(&sm.full[s], zb + qb);
-                    bulk_g2s_hint(sm.ring[s], reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(crow) * a.V + c0,
-                                  zb, &sm.full[s], stream_through);
-                    if (has_q)
-                        bulk_g2s_hint(sm.ring[s] + kResQOffset, a.q + static_cast<size_t>(cqrow) * a.V + c0, qb,
-                                      &sm.full[s], stream_through);
-                    ++k;
-                    if (st == 0 && pn < total_rb) {  // the next claim's decision, read ahead
-                        nb_req = decode_claim(pn, a).b;
-                        if (nb_req != cb) {
-                            nw0 = ld_relaxed_u64(a.fdec + 2 * nb_req);
-                            nw1 = ld_relaxed_u64(a.fdec + 2 * nb_req + 1);
-                        } else {
-                            nb_req = -1;
-                        }
+                if (pn < total_rb) {               // its decision, read ahead
+                    nb_req = decode_claim(pn, a).b;
+                    if (nb_req != cb) {
+                        nw0 = ld_relaxed_u64(a.fdec + 2 * nb_req);
+                        nw1 = ld_relaxed_u64(a.fdec + 2 * nb_req + 1);
+                    } else {
+                        nb_req = -1;
                     }
                 }
+                if (crow < 0) continue;  // invalid request: nothing to draw
+                if (!issue_claim(cl, crow, cqrow, cM, cinvS)) ok = false;
             }
             // end of stream (a phase without data), or wait for issued copies on abort
             int s;
@@ -2016,6 +2060,8 @@ static sv_status run_typed(Args &a, bool sample, bool vec, int small_nr, cudaStr
         const size_t per_position = static_cast<size_t>(a.B) * a.V * sizeof(T);
         const size_t keep = per_position ? (kL2KeepBytes / per_position) : 0;
         a.keep_rows = static_cast<int>(keep < static_cast<size_t>(kMaxRowsPerRequest) ? keep : kMaxRowsPerRequest);
+        // no row kept: start residual claims during the stats stream, while the selected rows are in L2
+        a.early_res = (sample && a.keep_rows == 0) ? 1 : 0;
     }
     if (a.B > kTicketCap &&
         cudaMemsetAsync(a.tickets1, 0, sizeof(uint32_t) * (static_cast<size_t>(a.B) + kSchedWords), s) !=

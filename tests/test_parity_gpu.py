@@ -164,6 +164,15 @@ def test_sampling_shapes(cuda_device, kernel, dtype, V, K, T):
     compare_sampling(f"sample V={V} K={K} T={T} {dtype} {kernel}", b.row_offsets, out, al, dg, _oracle(b))
 
 
+@pytest.mark.parametrize("dtype,V", [(torch.float32, 100000), (torch.bfloat16, 200000)])
+def test_sampling_batch_too_large_to_keep_rows(cuda_device, dtype, V):
+    """B x V x element size above a quarter of L2: no logits row is kept in L2
+    through the stats stream, and residual claims start during it."""
+    b = _rand_batch(77 + V, B=96, K=3, V=V, dtype=dtype, T=1.0)
+    out, al, dg = _gpu_fixed(b, cuda_device)
+    compare_sampling(f"sample B=96 K=3 V={V} {dtype} (early residual)", b.row_offsets, out, al, dg, _oracle(b))
+
+
 def test_sampling_k_zero_is_bonus_only(cuda_device, kernel):
     b = _rand_batch(5, B=40, K=0, V=3000, dtype=torch.float32, T=1.0)
     out, al, dg = _gpu_fixed(b, cuda_device)
