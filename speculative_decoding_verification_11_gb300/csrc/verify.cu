@@ -808,12 +808,14 @@ struct Tag {
     float M, invS;  // residual: the decision's normaliser
 };
 
+constexpr int kWorkerMassCap = 512;  // segment masses a draw keeps in registers and shared memory
 struct Smem {
     alignas(128) unsigned char ring[kStages][kChunkBytes];
     uint64_t full[kStages];
     uint64_t empty[kStages];
     Tag tag[kStages];
     int abort;
+    float wmass[kWorkerMassCap];  // the worker's copy of one request's segment masses (draw)
 };
 
 __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t *p) {
@@ -1076,7 +1078,7 @@ __device__ bool fused_decide(const Args &a, int b, int lane, volatile int *abort
 // gave up waiting.
 template <typename T>
 __device__ bool fused_draw(const Args &a, int b, const Sel &sel, float invS, int lane, volatile int *abort_flag,
-                           long long t_start) {
+                           long long t_start, float *wmass) {
     int r0, nr;
     request_rows(a, b, r0, nr);
     const T *zrow = reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(sel.row) * a.V;
@@ -1087,8 +1089,8 @@ __device__ bool fused_draw(const Args &a, int b, const Sel &sel, float invS, int
     const int ns = a.n_seg;
     const int G = (ns + 31) / 32;
     const int i0 = min(lane * G, ns), i1 = min(i0 + G, ns);
-    // this lane's masses stay in registers when they fit (V up to 131072)
-    constexpr int kRegSeg = 16;
+    // this lane's masses stay in registers (and in wmass) when they fit (V up to 131072)
+    constexpr int kRegSeg = kWorkerMassCap / 32;
     const bool in_regs = G <= kRegSeg;
     float mv[kRegSeg];
     for (;;) {
@@ -1108,14 +1110,13 @@ __device__ bool fused_draw(const Args &a, int b, const Sel &sel, float invS, int
         __nanosleep(kPollNs);
     }
     DS sum{0.f, 0.f};
-    float clo[kRegSeg];  // in registers: mv[i], clo[i] become the lane's inclusive sums (double-single)
     if (in_regs) {
 #pragma unroll
         for (int i = 0; i < kRegSeg; ++i) {
+            if (i0 + i < i1) wmass[i0 + i] = mv[i];
             sum = ds_add_f(sum, mv[i]);
-            mv[i] = sum.hi;
-            clo[i] = sum.lo;
         }
+        __syncwarp();
     } else {
         for (int i = i0; i < i1; ++i) sum = ds_add_f(sum, dec_mass(ld_relaxed_u32(mw + i)));
     }
@@ -1131,18 +1132,30 @@ __device__ bool fused_draw(const Args &a, int b, const Sel &sel, float invS, int
     DS t = ds_mul_f(R, u);
     int found = -1;
     DS fb{0.f, 0.f};
+    int fseg = -1;
+    DS fbase{0.f, 0.f};
     if (in_regs) {
-        // the first i whose inclusive sum passes t - P; compares independent of one another
-        const DS d = ds_add(t, DS{-P.hi, -P.lo});
-        DS prev{0.f, 0.f};
+        // The first lane whose running total passes t, then the first of its segments: its masses
+        // spread over lanes 0..G-1 (read back from shared memory) and one double-single scan.  (If none of them passes t, a rounding
+        // difference between the two sums: its last segment, whose in-segment scan then moves on.)
+        const unsigned lb = __ballot_sync(0xffffffffu, ds_gt(incl, t));
+        if (lb) {
+            const int L = __ffs(lb) - 1;
+            const int iL0 = min(L * G, ns), cnt = min(iL0 + G, ns) - iL0;
+            const float mine = lane < cnt ? wmass[iL0 + lane] : 0.f;
+            DS e{mine, 0.f};
 #pragma unroll
-        for (int i = 0; i < kRegSeg; ++i) {
-            const DS ci{mv[i], clo[i]};
-            if (found < 0 && i0 + i < i1 && ds_gt(ci, d)) {
-                found = i0 + i;
-                fb = ds_add(P, prev);
+            for (int o = 1; o < kRegSeg; o <<= 1) {
+                const DS y = ds_shfl_up(e, o);
+                if (lane >= o) e = ds_add(e, y);
             }
-            prev = ci;
+            DS ex = ds_shfl_up(e, 1);
+            if (lane == 0) ex = DS{0.f, 0.f};
+            const DS PL = ds_shfl(P, L);
+            const unsigned fl = __ballot_sync(0xffffffffu, lane < cnt && ds_gt(ds_add(PL, e), t));
+            const int j = fl ? __ffs(fl) - 1 : cnt - 1;
+            fseg = iL0 + j;
+            fbase = ds_add(PL, ds_shfl(ex, j));
         }
     } else {
         for (int i = i0; i < i1; ++i) {
@@ -1155,10 +1168,12 @@ __device__ bool fused_draw(const Args &a, int b, const Sel &sel, float invS, int
         }
     }
     for (int i = i0; i < i1; ++i) st_relaxed_u32(mw + i, 0u);  // consumed: leave the records zeroed
-    unsigned ball = __ballot_sync(0xffffffffu, found >= 0);
-    int src = ball ? (__ffs(ball) - 1) : 0;
-    int fseg = ball ? __shfl_sync(0xffffffffu, found, src) : -1;
-    DS fbase = ds_shfl(fb, src);
+    if (!in_regs) {
+        const unsigned ball = __ballot_sync(0xffffffffu, found >= 0);
+        const int src = ball ? (__ffs(ball) - 1) : 0;
+        fseg = ball ? __shfl_sync(0xffffffffu, found, src) : -1;
+        fbase = ds_shfl(fb, src);
+    }
     if (!(R.hi > 0.f)) {
         // empty residual after a rejection: draw from p instead (slow path, one segment at a time)
         qrow = nullptr;
@@ -1481,7 +1496,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                 if (sel.valid) publish_decision(a.fdec + 2 * b, sel.M, invS, sel.row, sel.qrow);
                 else publish_decision(a.fdec + 2 * b, 0.f, 1.f, -1, -1);
             }
-            if (sel.valid && !fused_draw<T>(a, b, sel, invS, lane, abort_flag, t_start)) break;
+            if (sel.valid && !fused_draw<T>(a, b, sel, invS, lane, abort_flag, t_start, sm.wmass)) break;
         }
     } else {
         // consumers
