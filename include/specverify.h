@@ -306,6 +306,18 @@ int spec_last_launch_count(void);
 size_t spec_set_small_kernel_limit(size_t bytes);
 
 /*
+ * Kernel choice for small batches of medium requests.  With `enable` non-zero
+ * (the default), a call on 16-byte aligned rows (and q) that the small kernel
+ * does not take runs one cluster of 8 CTAs per request when the request has
+ * at most 16 rows, B <= 64, B x 8 CTAs fit twice over the GPU's SMs, V <=
+ * 131072 and each CTA's slice of the request's rows fits in 100 KB of shared
+ * memory; otherwise the call streams through the persistent kernel.  Both
+ * compute the same step.  Process-wide (an atomic); returns the previous
+ * setting (0 or 1).  A tuning knob of this library, like the one above.
+ */
+int spec_set_cluster_kernel(int enable);
+
+/*
  * Paged KV-cache bookkeeping around verification ("Speculative Decoding in
  * Large Language Models", section 4, "Segmented Block Allocation
  * (PagedAttention)": fixed-size blocks, block pointers for the speculative

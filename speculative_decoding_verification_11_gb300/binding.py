@@ -26,7 +26,8 @@ EXPORTS = (
     "spec_verify_workspace_size", "spec_verify_greedy", "spec_verify_sample", "spec_verify_ragged",
     "spec_lmhead_workspace_size", "spec_lmhead_verify", "spec_verify_last_device_status",
     "spec_status_string", "spec_profile_set_events", "spec_last_launch_count",
-    "spec_verify_sample_noalloc", "spec_set_small_kernel_limit", "spec_kv_reserve", "spec_kv_rollback",
+    "spec_verify_sample_noalloc", "spec_set_small_kernel_limit", "spec_set_cluster_kernel",
+    "spec_kv_reserve", "spec_kv_rollback",
     "spec_draft_workspace_size", "spec_draft_sample", "spec_ngram_draft", "spec_dynk_update",
 )
 
@@ -68,6 +69,7 @@ def load() -> ctypes.CDLL:
             "spec_last_launch_count": (I, []),
             "spec_verify_sample_noalloc": (I, [P, I, P, I, I, I, F, P, P, P, P, P, P]),
             "spec_set_small_kernel_limit": (Z, [Z]),
+            "spec_set_cluster_kernel": (I, [I]),
             "spec_kv_reserve": (I, [P, P, P, P, P, I, I, I, P, P]),
             "spec_kv_rollback": (I, [P, P, P, P, P, P, I, I, I, I, P, P]),
             "spec_draft_workspace_size": (Z, [I, I, I]),
@@ -264,6 +266,12 @@ def spec_set_small_kernel_limit(nbytes: int) -> int:
     request-per-CTA kernel; 0 sends every call to the streaming kernel.
     Returns the previous value."""
     return int(load().spec_set_small_kernel_limit(int(nbytes)))
+
+
+def spec_set_cluster_kernel(enable: bool) -> bool:
+    """Whether small batches of medium requests may run one cluster of CTAs
+    per request.  Returns the previous setting."""
+    return bool(load().spec_set_cluster_kernel(1 if enable else 0))
 
 
 def _check_kv(block_table, seq_len, free_ids, free_count, status):

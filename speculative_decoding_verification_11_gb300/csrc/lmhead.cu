@@ -715,6 +715,7 @@ __global__ void __launch_bounds__(kFinThreads, 2) verify_finish_kernel(const flo
                                                                     const float *uniforms, int32_t *out_tokens,
                                                                     int32_t *accept_len, float *diag,
                                                                     uint32_t *status, float *seg_scratch, int B) {
+    cluster_arrive_relaxed();  // waited on before the first remote store
     pdl_wait_prior_grid();  // the spill and the partials come from the GEMM before it
     pdl_launch_dependents();
     const uint32_t rank = cluster_ctarank();
@@ -805,6 +806,7 @@ __global__ void __launch_bounds__(kFinThreads, 2) verify_finish_kernel(const flo
     __syncthreads();
     // every CTA of the cluster has the same ks: leaving together touches no other CTA's memory
     if (!kSample || s_ks < 0) return;
+    cluster_wait();  // every CTA of the cluster is running: remote stores below are safe
 
     const int ks = s_ks;
     const float M = s_row[ks].x, invS = 1.f / s_row[ks].y;

@@ -228,6 +228,14 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     return r;
 }
 
+// Split cluster barrier: every thread arrives as the kernel starts and waits
+// before its first access to another CTA's shared memory, which is only valid
+// once every CTA of the cluster is running.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
 // Whole-cluster barrier; release/acquire orders shared-memory writes before it
 // with distributed-shared-memory reads after it.
 __device__ __forceinline__ void cluster_sync() {

@@ -45,15 +45,18 @@ def _gpu_ragged(batch, dev, T=None, diag=True):
     return out.cpu().numpy(), al.cpu().numpy(), (dg.cpu().numpy() if dg is not None else None)
 
 
-@pytest.fixture(params=["small", "stream"])
+@pytest.fixture(params=["small", "stream", "cluster"])
 def kernel(request, cuda_device):
     """Runs a test on each kernel: "small" raises the request-per-CTA kernel's
     limit to 192 KB of logits per request (so that every shape that fits its
     shared memory takes it), "stream" sends every call to the persistent
-    streaming kernel."""
+    streaming kernel, "cluster" lets every shape the cluster-per-request
+    kernel takes run on it (the others stream)."""
     prev = B_.spec_set_small_kernel_limit(192 * 1024 if request.param == "small" else 0)
+    prev_c = B_.spec_set_cluster_kernel(request.param != "stream")
     yield request.param
     B_.spec_set_small_kernel_limit(prev)
+    B_.spec_set_cluster_kernel(prev_c)
 
 
 def _status(dev):
