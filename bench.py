@@ -573,29 +573,38 @@ def run_config(args):
     ws = B_.workspace(B_.spec_verify_workspace_size(Bn, R, V), dev)
     in_bytes = sum(t.numel() * t.element_size() for t in (logits, q) if t is not None)
     small = in_bytes < 2 * (129 << 20)
+    # inputs smaller than twice L2: steps rotate over enough copies that no step finds the bytes
+    # an earlier step read in L2 (or, with --l2-flush, L2 is flushed before every timed call)
+    n_copies = 1 if (not small or args.l2_flush) else -(-2 * (129 << 20) // in_bytes) + 1
+    copies = [(logits, q)] + [(logits.clone(), q.clone() if q is not None else None) for _ in range(n_copies - 1)]
+    k_step = [0]
 
     def step():
+        lg, qq = copies[k_step[0] % n_copies]
+        k_step[0] += 1
         if args.config == "greedy":
-            B_.spec_verify_greedy(logits, draft, Bn, batch.K, V, out, al, ws, stream=stream)
+            B_.spec_verify_greedy(lg, draft, Bn, batch.K, V, out, al, ws, stream=stream)
         elif args.config == "ragged":
-            B_.spec_verify_ragged(logits, q, offs, Bn, R, V, batch.temperature, draft, uni, out, al, ws,
+            B_.spec_verify_ragged(lg, qq, offs, Bn, R, V, batch.temperature, draft, uni, out, al, ws,
                                   stream=stream)
         else:
-            B_.spec_verify_sample(logits, q, Bn, batch.K, V, batch.temperature, draft, uni, out, al, ws,
+            B_.spec_verify_sample(lg, qq, Bn, batch.K, V, batch.temperature, draft, uni, out, al, ws,
                                   stream=stream)
 
     # inputs that fit in L2 are evicted before every timed call: a 256 MB write,
     # then a 256 MB read so that no dirty line is left to be written back inside
     # the timed call
-    fw = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if small else None
-    fr = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if small else None
-    for _ in range(max(args.warmup, 3)):
+    flush = small and args.l2_flush
+    fw = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    fr = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    for _ in range(max(args.warmup, 3, n_copies)):
         step()
     torch.cuda.synchronize()
     n0 = B_.spec_last_launch_count()
+    kernel_used = B_.spec_last_kernel()
     clocks = Clocks(0)
     clocks.start()
-    if small:
+    if flush:
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
         for i in range(args.steps):
@@ -615,7 +624,8 @@ def run_config(args):
         e1.record(stream)
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / args.steps
-        l2 = f"inputs {in_bytes / 1e6:.1f} MB > L2 (129 MB), no flush: calls back to back"
+        l2 = (f"inputs {in_bytes / 1e6:.1f} MB > L2 (129 MB), no flush: calls back to back" if not small else
+              f"inputs {in_bytes / 1e6:.1f} MB x {n_copies} rotating copies > 2 x L2, no flush: calls back to back")
     clk = clocks.stop()
     alg = _alg_bytes(batch, al, R)
     drafts = R - Bn
@@ -628,7 +638,9 @@ def run_config(args):
         "dtype": "bf16" if logits.dtype == torch.bfloat16 else "f32", "data": "synthetic",
         "config": {"workload": f"{args.config} verify B={Bn} rows={R} V={V} T={batch.temperature}", "l2": l2},
         "mean_accept_len": float(al.float().mean()),
-        "roofline": {"kernel": "fused_kernel (whole step)", "bound": "hbm", "achieved": achieved, "peak": peak,
+        "roofline": {"kernel": {"small": "sk::small_kernel", "cluster": "cv::cluster_kernel", "stream": "fused_kernel",
+                                "scalar": "stats_scalar_kernel + residual_kernel"}.get(kernel_used, kernel_used) +
+                               " (whole step)", "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
                      "algorithmic_bytes_per_launch": alg, "ms_per_launch": ms},
         "clocks": clk, "gpu_launches": args.steps * n0,

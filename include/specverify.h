@@ -293,6 +293,15 @@ sv_status spec_profile_set_events(void *begin, void *end);
 int spec_last_launch_count(void);
 
 /*
+ * Which verification kernel the last spec_verify_greedy / _sample / _ragged /
+ * _sample_noalloc call on this thread chose: "small" (one CTA per request),
+ * "cluster" (one cluster of CTAs per request), "stream" (the persistent
+ * streaming kernel), "scalar" (rows not 16-byte aligned: element loads, two
+ * passes), or "none" before any such call.  A static string; for accounting.
+ */
+const char *spec_last_kernel(void);
+
+/*
  * Kernel choice for small vocabularies.  A call of spec_verify_greedy,
  * spec_verify_sample, spec_verify_ragged or spec_verify_sample_noalloc whose
  * requests each hold at most `bytes` of logits ((rows per request) x V x

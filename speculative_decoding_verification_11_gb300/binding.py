@@ -25,7 +25,7 @@ SV_MAX_K = 255
 EXPORTS = (
     "spec_verify_workspace_size", "spec_verify_greedy", "spec_verify_sample", "spec_verify_ragged",
     "spec_lmhead_workspace_size", "spec_lmhead_verify", "spec_verify_last_device_status",
-    "spec_status_string", "spec_profile_set_events", "spec_last_launch_count",
+    "spec_status_string", "spec_profile_set_events", "spec_last_launch_count", "spec_last_kernel",
     "spec_verify_sample_noalloc", "spec_set_small_kernel_limit", "spec_set_cluster_kernel",
     "spec_kv_reserve", "spec_kv_rollback",
     "spec_draft_workspace_size", "spec_draft_sample", "spec_ngram_draft", "spec_dynk_update",
@@ -67,6 +67,7 @@ def load() -> ctypes.CDLL:
             "spec_status_string": (ctypes.c_char_p, [I]),
             "spec_profile_set_events": (I, [P, P]),
             "spec_last_launch_count": (I, []),
+            "spec_last_kernel": (ctypes.c_char_p, []),
             "spec_verify_sample_noalloc": (I, [P, I, P, I, I, I, F, P, P, P, P, P, P]),
             "spec_set_small_kernel_limit": (Z, [Z]),
             "spec_set_cluster_kernel": (I, [I]),
@@ -362,6 +363,12 @@ def spec_dynk_update(accept_len, k_used, hist, count, policy, k_low, k_high, k_n
 
 def spec_last_launch_count() -> int:
     return int(load().spec_last_launch_count())
+
+
+def spec_last_kernel() -> str:
+    """The verification kernel the last verify call on this thread chose:
+    "small", "cluster", "stream", "scalar" or "none"."""
+    return load().spec_last_kernel().decode()
 
 
 def workspace(nbytes: int, device=None) -> torch.Tensor:

@@ -2033,48 +2033,55 @@ __global__ void __launch_bounds__(kThreads, 2) cluster_kernel(Args a) {
             const int nq = nt >> 2;  // 4-token groups of the slice
             const int q0 = (nq * part) / wpr, q1 = (nq * (part + 1)) / wpr;
             const T *row = zs + static_cast<size_t>(j) * slice;
+            // four independent accumulators (one per position within a 4-token group) and
+            // several groups' loads in flight: the loops are latency-bound otherwise
             if (kSample) {
-                float zmax = -INFINITY;
+                float zm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 4
                 for (int i = q0 + lane; i < q1; i += 32) {
                     float z[4];
                     load4<T>(row + 4 * i, z);
-                    zmax = fmaxf(fmaxf(zmax, fmaxf(z[0], z[1])), fmaxf(z[2], z[3]));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) zm[k] = fmaxf(zm[k], z[k]);
                 }
-                zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 16));
-                zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 8));
-                zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 4));
-                zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 2));
-                zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 1));
+                float zmax = fmaxf(fmaxf(zm[0], zm[1]), fmaxf(zm[2], zm[3]));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
                 if (zmax != -INFINITY) {
                     const float Mw = __fmul_rn(zmax, a.c);  // c > 0: the max of c z
-                    float s = 0.f;
+                    float sk[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
                     for (int i = q0 + lane; i < q1; i += 32) {
                         float z[4];
                         load4<T>(row + 4 * i, z);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) s += ex2(__fmaf_rn(z[k], a.c, -Mw));
+                        for (int k = 0; k < 4; ++k) sk[k] += ex2(__fmaf_rn(z[k], a.c, -Mw));
                     }
+                    float s = (sk[0] + sk[1]) + (sk[2] + sk[3]);
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
                     ra = Mw;
                     rb = __float_as_int(s);
                 }
             } else {
-                float bv = -INFINITY;
-                int bi = 0x7fffffff;
+                float bv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                int bi[4] = {0x7fffffff, 0x7fffffff, 0x7fffffff, 0x7fffffff};
+#pragma unroll 4
                 for (int i = q0 + lane; i < q1; i += 32) {
                     float z[4];
                     load4<T>(row + 4 * i, z);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        if (z[k] > bv) {  // strict: the lowest index of this lane's maxima
-                            bv = z[k];
-                            bi = t0 + 4 * i + k;
+                        if (z[k] > bv[k]) {  // strict: each stream keeps the lowest index of its maxima
+                            bv[k] = z[k];
+                            bi[k] = t0 + 4 * i + k;
                         }
                 }
-                warp_am_reduce(bv, bi);
-                ra = bv;
-                rb = bi;
+#pragma unroll
+                for (int k = 1; k < 4; ++k) am_merge(bv[0], bi[0], bv[k], bi[k]);  // lower index on equal values
+                warp_am_reduce(bv[0], bi[0]);
+                ra = bv[0];
+                rb = bi[0];
             }
         }
         if (lane == 0) s_wpart[warp] = make_float2(ra, __int_as_float(rb));
@@ -2419,6 +2426,7 @@ static void set_ws_records(Args &a, char *w, const WsLayout &L) {
 static void *g_prof_begin = nullptr;
 static void *g_prof_end = nullptr;
 static thread_local int g_last_launches = 0;
+static thread_local const char *g_last_kernel = "none";
 
 void prof_begin(cudaStream_t s) {
     if (g_prof_begin) cudaEventRecord(static_cast<cudaEvent_t>(g_prof_begin), s);
@@ -2588,6 +2596,7 @@ static sv_status run_typed(Args &a, bool sample, bool vec, int small_nr, int clu
         ++launches;
     }
     prof_begin(s);
+    g_last_kernel = small_nr > 0 ? "small" : cluster_nr > 0 ? "cluster" : vec ? "stream" : "scalar";
     if (small_nr > 0) {
         // small vocabulary: one CTA per request, everything in shared memory
         const cudaError_t e = sample ? launch_small<T, true>(a, small_nr, s) : launch_small<T, false>(a, small_nr, s);
@@ -2827,6 +2836,8 @@ extern "C" sv_status spec_profile_set_events(void *begin, void *end) {
 }
 
 extern "C" int spec_last_launch_count(void) { return g_last_launches; }
+
+extern "C" const char *spec_last_kernel(void) { return g_last_kernel; }
 
 extern "C" int spec_set_cluster_kernel(int enable) {
     return g_cluster_on.exchange(enable != 0 ? 1 : 0, std::memory_order_relaxed);
