@@ -44,8 +44,9 @@ def _peaks():
 
 # the sources each profiled kernel is built from (its own file and the shared device headers)
 KERNEL_SOURCES = {
-    "fused_kernel": ("verify.cu", "sv_device.cuh", "sv_draw.cuh", "sv_host.h"),
+    "fused_kernel": ("verify.cu", "sv_args.cuh", "sv_device.cuh", "sv_draw.cuh", "sv_host.h"),
     "lmhead_gemm_kernel": ("lmhead.cu", "sv_device.cuh", "sv_draw.cuh", "sv_host.h"),
+    "cluster_kernel": ("cluster.cu", "sv_args.cuh", "sv_device.cuh", "sv_draw.cuh", "sv_host.h"),
 }
 
 
@@ -641,7 +642,11 @@ def run_config(args):
         "roofline": {"kernel": {"small": "sk::small_kernel", "cluster": "cv::cluster_kernel", "stream": "fused_kernel",
                                 "scalar": "stats_scalar_kernel + residual_kernel"}.get(kernel_used, kernel_used) +
                                " (whole step)", "bound": "hbm", "achieved": achieved, "peak": peak,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     # the committed capture of the cluster kernel is of this greedy workload; no other
+                     # secondary workload has one
+                     "traffic": _traffic("cluster_kernel") if (args.config == "greedy" and kernel_used == "cluster")
+                     else None,
                      "algorithmic_bytes_per_launch": alg, "ms_per_launch": ms},
         "clocks": clk, "gpu_launches": args.steps * n0,
     }

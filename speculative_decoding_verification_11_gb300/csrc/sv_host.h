@@ -19,4 +19,7 @@ sv_status finish_from_partials(const float *logits, const float2 *partials, int 
                                int K, int V, float temperature, bool sample, const int32_t *draft,
                                const float *uniforms, int32_t *out_tokens, int32_t *accept_len, float *diag,
                                void *ws, size_t ws_bytes, cudaStream_t s, int *launches);
+struct Args;
+// One cluster of CTAs per request over the call in `a` (cluster.cu); nr_cap rows per request at most.
+cudaError_t launch_cluster_kernel(const Args &a, int nr_cap, bool sample, bool bf16, cudaStream_t s);
 }  // namespace sv
