@@ -76,6 +76,7 @@ struct LmArgs {
     int M, d, V, n_tiles;
     float c;          // log2(e) / T
     float *spill;     // M x V fp32 logits (sampling), or nullptr
+    int spill_keep;   // 1: the spill is scratch read back from L2 soon (stores at evict_last priority)
     float2 *partials; // M x gridDim.x: one merged partial per row and CTA
     uint32_t *status;
 };
@@ -262,6 +263,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
         const int row = quad * 32 + lane;
         const bool live = row < a.M;
         const bool vec_store = (a.V & 3) == 0;
+        const uint64_t keep_pol = l2_evict_last_policy();
         // running partial of this row over every tile of the CTA
         float Mr = -INFINITY, Sr = 0.f;
         float bv = -INFINITY;
@@ -296,7 +298,10 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                         Mr = Mn;
                     }
                     float *dst = a.spill + static_cast<size_t>(row) * a.V + col0;
-                    if (vec_store && nvalid == 32) {
+                    if (vec_store && nvalid == 32 && a.spill_keep) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) st_f32x4_hint(dst + i, v[i], v[i + 1], v[i + 2], v[i + 3], keep_pol);
+                    } else if (vec_store && nvalid == 32) {
 #pragma unroll
                         for (int i = 0; i < 32; i += 4)
                             *reinterpret_cast<float4 *>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
@@ -875,7 +880,16 @@ __global__ void __launch_bounds__(kFinThreads, 2) verify_finish_kernel(const flo
         }
         break;
     }
-    if (warp != 0) return;
+    if (warp != 0) {
+        // every CTA's gathers are behind the barrier: the other rows' slices are read by nobody
+        // again, so warps 1.. drop their L2 lines unwritten while warp 0 draws
+        const int t1 = min(seg1 * kSegElems, V), t0s = seg0 * kSegElems;
+        for (int j = 0; j < nr; ++j)
+            if (j != ks && t1 > t0s)
+                discard_l2_range(spill + static_cast<size_t>(r0 + j) * V + t0s, spill + static_cast<size_t>(r0 + j) * V + t1,
+                                 tid - 32, kFinThreads - 32);
+        return;
+    }
 
     // prefix of the slice totals, R, u R and the CTA whose slice holds u R
     const float u = __ldg(uniforms + r0 + K);
@@ -996,14 +1010,17 @@ extern "C" sv_status spec_lmhead_verify(const void *hidden, const void *w_vocab_
     a.spill = sample ? reinterpret_cast<float *>(w + L.spill) : nullptr;
     a.partials = reinterpret_cast<float2 *>(w + L.partials);
     a.status = reinterpret_cast<uint32_t *>(w + L.finish);  // the status word is the workspace's first word
+    // the cluster finish reads back only the selected rows and discards the rest from L2
+    const bool cluster_finish = V % 4 == 0 && lm::fin_segs_per_cta(V) <= lm::kFinMaxSegs &&
+                                (!sample || K == 0 || (reinterpret_cast<uintptr_t>(q) & 15u) == 0);
+    a.spill_keep = (sample && cluster_finish) ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     prof_begin(s);
     if (sample) lm::launch_gemm_bn<true>(bn, ta, tb, a, grid, s);
     else lm::launch_gemm_bn<false>(bn, ta, tb, a, grid, s);
     prof_end(s);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
-    if (V % 4 == 0 && lm::fin_segs_per_cta(V) <= lm::kFinMaxSegs &&
-        (!sample || K == 0 || (reinterpret_cast<uintptr_t>(q) & 15u) == 0)) {
+    if (cluster_finish) {
         // one cluster of kFinC CTAs per request over the spill and the partials
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(lm::kFinC, B);
@@ -1080,6 +1097,7 @@ extern "C" sv_status spec_draft_sample(const void *hidden, const void *w_vocab_t
     a.n_tiles = n_tiles;
     a.c = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(temperature)) : 1.f;
     a.spill = sample ? q_out : nullptr;  // the logits land in q's buffer, turned into q in place
+    a.spill_keep = 0;                    // an output: plain stores
     a.partials = reinterpret_cast<float2 *>(w + 256);
     a.status = reinterpret_cast<uint32_t *>(w);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
