@@ -76,7 +76,7 @@ struct LmArgs {
     int M, d, V, n_tiles;
     float c;          // log2(e) / T
     float *spill;     // M x V fp32 logits (sampling), or nullptr
-    int spill_keep;   // 1: the spill is scratch read back from L2 soon (stores at evict_last priority)
+    int spill_keep;   // 1: the spill is read back from L2 soon (stores at evict_last priority)
     float2 *partials; // M x gridDim.x: one merged partial per row and CTA
     uint32_t *status;
 };
@@ -1097,7 +1097,7 @@ extern "C" sv_status spec_draft_sample(const void *hidden, const void *w_vocab_t
     a.n_tiles = n_tiles;
     a.c = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(temperature)) : 1.f;
     a.spill = sample ? q_out : nullptr;  // the logits land in q's buffer, turned into q in place
-    a.spill_keep = 0;                    // an output: plain stores
+    a.spill_keep = 1;                    // read back and rewritten as q by the finish kernel, from L2
     a.partials = reinterpret_cast<float2 *>(w + 256);
     a.status = reinterpret_cast<uint32_t *>(w);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
