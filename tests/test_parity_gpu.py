@@ -357,3 +357,29 @@ def test_one_workspace_serves_calls_of_any_shape(cuda_device):
             B_.spec_verify_sample(*args, o2, a2, B_.workspace(B_.spec_verify_workspace_size(b.B, b.rows, b.V), dev))
             torch.cuda.synchronize()
             assert torch.equal(o1, o2) and torch.equal(a1, a2), (rep, b.B, b.K, b.V)
+
+
+def test_kernel_choice_follows_the_knobs(cuda_device):
+    """The path a call takes, as spec_last_kernel() reports it, follows the
+    size rules and the two process-wide knobs; every path gives the oracle's
+    result (checked above), so this pins only the dispatch."""
+    dev = cuda_device
+    prev_s = B_.spec_set_small_kernel_limit(48 * 1024)
+    prev_c = B_.spec_set_cluster_kernel(True)
+    try:
+        def kind(V, K, B, dtype=torch.float32):
+            b = _rand_batch(3 + V, B=B, K=K, V=V, dtype=dtype, T=1.0)
+            _gpu_fixed(b, dev)
+            return B_.spec_last_kernel()
+
+        assert kind(1024, 4, 8) == "small"                 # 20 KB of logits per request
+        assert kind(32000, 5, 16) == "cluster"             # 768 KB per request, 16 requests
+        assert kind(32000, 5, 64) == "stream"              # 64 x 8 CTAs exceed two per SM
+        assert kind(4097, 3, 8) == "scalar"                # rows not 16-byte aligned
+        B_.spec_set_cluster_kernel(False)
+        assert kind(32000, 5, 16) == "stream"
+        B_.spec_set_small_kernel_limit(0)
+        assert kind(1024, 4, 8) == "stream"
+    finally:
+        B_.spec_set_small_kernel_limit(prev_s)
+        B_.spec_set_cluster_kernel(prev_c)
