@@ -84,6 +84,23 @@ struct LmArgs {
 // ---------------------------------------------------------------------------
 // PTX wrappers
 // ---------------------------------------------------------------------------
+// 16-byte global store with an L2 eviction-priority policy.
+__device__ __forceinline__ void st_f32x4_hint(float *p, float a, float b, float c, float d, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(a), "f"(b), "f"(c),
+                 "f"(d), "l"(pol)
+                 : "memory");
+}
+
+// Invalidate the 128-byte L2 lines that lie wholly inside [begin, end) without
+// writing them back (their contents become indeterminate); thread i of n takes
+// lines i, i + n, ...  For scratch that nobody reads again.
+__device__ __forceinline__ void discard_l2_range(const void *begin, const void *end, int i, int n) {
+    const uintptr_t b = (reinterpret_cast<uintptr_t>(begin) + 127u) & ~static_cast<uintptr_t>(127u);
+    const uintptr_t e = reinterpret_cast<uintptr_t>(end) & ~static_cast<uintptr_t>(127u);
+    for (uintptr_t l = b + static_cast<uintptr_t>(i) * 128u; l < e; l += static_cast<uintptr_t>(n) * 128u)
+        asm volatile("discard.global.L2 [%0], 128;" ::"l"(l) : "memory");
+}
+
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
 // 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), sm_100 form.
 __device__ __forceinline__ uint64_t smem_desc_sw128(const void *p) {
