@@ -1229,7 +1229,23 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
     // this workspace) are visible only after this wait.
     pdl_wait_prior_grid();
     pdl_launch_dependents();
-    if (a.csr_ok && !__ldcg(a.csr_ok)) return;
+    if (a.row_offsets) {
+        // the CSR offsets are checked here, by every CTA (the same verdict in each), instead of by a
+        // kernel of their own ahead of this one: offsets[0] = 0, offsets[B] = rows, 1..256 rows each
+        bool bad = tid == 0 && (__ldg(a.row_offsets) != 0 || __ldg(a.row_offsets + a.B) != a.rows);
+        for (int b = tid; b < a.B; b += kThreads) {
+            const int k1 = __ldg(a.row_offsets + b + 1) - __ldg(a.row_offsets + b);
+            bad |= (k1 < 1 || k1 > kMaxRowsPerRequest);
+        }
+        if (__syncthreads_or(bad)) {
+            if (blockIdx.x == 0) {
+                for (int b = tid; b < a.B; b += kThreads) a.accept_len[b] = 0;
+                for (int r = tid; r < a.rows; r += kThreads) a.out_tokens[r] = -1;
+                if (tid == 0) atomicOr(a.status, SV_FLAG_BAD_OFFSETS);
+            }
+            return;
+        }
+    }
     volatile int *abort_flag = &sm.abort;
     const long long t_start = clock64();
     auto timeout = [&]() {
@@ -1255,7 +1271,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
             // (acceptance decays with position, so the earliest drafts are the likeliest to be rejected):
             // its first keep_rows rows are loaded at normal priority (keep_rows sized on the host to a
             // quarter of L2), every other stats row and every residual read as evict_first, so the kept
-            // rows outlive the stream without outliving the step's successors.
+            // rows outlive the stream without outliving the step's successors.  With early residual
+            // claims (no row kept) every stats row loads at normal priority: its request's residual
+            // claim comes a few microseconds later, and evict_first lines would be gone by then.
             const uint64_t keep = l2_evict_normal_policy(), stream_through = l2_evict_first_policy();
             int jn = static_cast<int>(atomicAdd(a.sched + 0, 1u));
             uint32_t pn = 0xffffffffu;     // next residual claim (in flight)
@@ -1343,7 +1361,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                         mbar_arrive_expect_tx(&sm.full[s], bytes);
                         bulk_g2s_hint(sm.ring[s],
                                       reinterpret_cast<const T *>(a.logits) + static_cast<size_t>(row) * a.V + c0, bytes,
-                                      &sm.full[s], first_row ? keep : stream_through);
+                                      &sm.full[s], (first_row || a.early_res) ? keep : stream_through);
                         ++k;
                     }
                     continue;
@@ -2032,7 +2050,8 @@ static sv_status run_typed(Args &a, bool sample, bool vec, int small_nr, int clu
         cudaMemsetAsync(a.tickets1, 0, sizeof(uint32_t) * (static_cast<size_t>(a.B) + kSchedWords), s) !=
             cudaSuccess)
         return SV_ERR_CUDA;
-    if (a.row_offsets) {
+    const bool fused = small_nr == 0 && cluster_nr == 0 && vec;  // checks the offsets itself
+    if (a.row_offsets && !fused) {
         csr_check_kernel<<<1, kThreads, 0, s>>>(a, const_cast<int *>(a.csr_ok));
         ++launches;
     }
