@@ -48,6 +48,7 @@ KERNEL_SOURCES = {
     "lmhead_gemm_kernel": ("lmhead.cu", "sv_device.cuh", "sv_draw.cuh", "sv_host.h"),
     "cluster_kernel": ("cluster.cu", "sv_args.cuh", "sv_device.cuh", "sv_draw.cuh", "sv_host.h"),
 }
+KERNEL_SOURCES["fused_kernel_ragged"] = KERNEL_SOURCES["fused_kernel"]  # the same kernel, its ragged capture
 
 
 def _source_hash(kernel: str):
@@ -665,10 +666,11 @@ def run_config(args):
                                 "scalar": "stats_scalar_kernel + residual_kernel"}.get(kernel_used, kernel_used) +
                                " (whole step)", "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     # the committed capture of the cluster kernel is of this greedy workload; no other
-                     # secondary workload has one
-                     "traffic": _traffic("cluster_kernel") if (args.config == "greedy" and kernel_used == "cluster")
-                     else None,
+                     # committed captures exist for the greedy workload (cluster kernel) and the ragged
+                     # one (streaming kernel); tiny has none
+                     "traffic": (_traffic("cluster_kernel") if (args.config == "greedy" and kernel_used == "cluster")
+                                 else _traffic("fused_kernel_ragged") if (args.config == "ragged" and kernel_used == "stream")
+                                 else None),
                      "algorithmic_bytes_per_launch": alg, "ms_per_launch": ms},
         "clocks": clk, "gpu_launches": args.steps * n0,
     }
