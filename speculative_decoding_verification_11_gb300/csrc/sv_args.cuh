@@ -88,4 +88,23 @@ __host__ __device__ constexpr size_t smem_bytes(int nr_cap, int V, int esize) {
 
 }  // namespace cv
 
+namespace sk {
+
+// One CTA per request, the request's rows in shared memory (small.cu).
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr size_t kDefaultRowBytes = 48 * 1024;
+constexpr size_t kMaxSmemBytes = 200 * 1024;  // largest dynamic shared memory a launch may ask for
+
+__host__ __device__ constexpr size_t a16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+
+// Dynamic shared memory: rows (nr_cap x V elements) | row normalisers (8 B
+// per row) | residual row (4 B per token) | per-thread sums (8 B per thread).
+__host__ __device__ constexpr size_t smem_bytes(int nr_cap, int V, int esize) {
+    return a16(static_cast<size_t>(nr_cap) * V * esize) + a16(static_cast<size_t>(nr_cap) * 8) +
+           a16(static_cast<size_t>(V) * 4) + kThreads * 8;
+}
+
+}  // namespace sk
+
 }  // namespace sv

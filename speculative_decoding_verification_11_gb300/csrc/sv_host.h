@@ -22,4 +22,6 @@ sv_status finish_from_partials(const float *logits, const float2 *partials, int 
 struct Args;
 // One cluster of CTAs per request over the call in `a` (cluster.cu); nr_cap rows per request at most.
 cudaError_t launch_cluster_kernel(const Args &a, int nr_cap, bool sample, bool bf16, cudaStream_t s);
+// One CTA per request over the call in `a` (small.cu); nr_cap rows per request at most.
+cudaError_t launch_small_kernel(const Args &a, int nr_cap, bool sample, bool bf16, cudaStream_t s);
 }  // namespace sv
