@@ -383,3 +383,40 @@ def test_kernel_choice_follows_the_knobs(cuda_device):
     finally:
         B_.spec_set_small_kernel_limit(prev_s)
         B_.spec_set_cluster_kernel(prev_c)
+
+
+@pytest.mark.parametrize("V", [4096, 20000])
+def test_empty_residual_on_aligned_rows(cuda_device, kernel, V):
+    """q = 1 everywhere: every draft is rejected and every residual is empty,
+    so each request draws from p and the call sets the flag; on all paths
+    (the cluster kernel's retry included), against the oracle."""
+    dev = cuda_device
+    b = _rand_batch(900 + V, B=6, K=2, V=V, dtype=torch.float32, T=1.0)
+    b = W.Batch(b.name, b.logits, torch.ones_like(b.q), b.draft, b.uniforms, b.row_offsets, b.B, b.K, b.V,
+                b.temperature)
+    _gpu_fixed(b, dev)
+    _status(dev)  # clears the status word of the call's workspace
+    out, al, dg = _gpu_fixed(b, dev)
+    compare_sampling(f"empty residual V={V} {kernel}", b.row_offsets, out, al, dg, _oracle(b))
+    st, flags = _status(dev)
+    assert st == B_.SV_OK and flags & B_.SV_FLAG_ZERO_RESIDUAL
+
+
+def test_residual_at_one_token_is_drawn(cuda_device, kernel):
+    """q = 1 except q(t) = 0 at one token t per request: the draft is rejected
+    and r > 0 at t alone, so t is drawn whatever the uniform.  The targets lie
+    in different slices of the cluster kernel, on both sides of a slice
+    boundary (2560 tokens at V = 20000) and in the ragged last segment."""
+    dev = cuda_device
+    V = 20000
+    targets = [5, 2559, 2560, 7777, 12345, 17999, 19968, 19999]
+    b = _rand_batch(77, B=len(targets), K=1, V=V, dtype=torch.float32, T=1.0)
+    q = torch.ones_like(b.q)
+    for i, t in enumerate(targets):
+        q[i, t] = 0.0
+    b = W.Batch(b.name, b.logits, q, b.draft, b.uniforms, b.row_offsets, b.B, b.K, b.V, b.temperature)
+    out, al, dg = _gpu_fixed(b, dev)
+    for i, t in enumerate(targets):
+        if int(b.draft[i]) != t:
+            assert al[i] == 1 and out[2 * i] == t, (kernel, i, t, al[i], out[2 * i])
+    compare_sampling(f"one-token residual V={V} {kernel}", b.row_offsets, out, al, dg, _oracle(b))
