@@ -45,8 +45,8 @@ def _peaks():
 # the sources each profiled kernel is built from (its own file and the shared device headers)
 KERNEL_SOURCES = {
     "fused_kernel": ("verify.cu", "sv_args.cuh", "sv_device.cuh", "sv_draw.cuh", "sv_host.h"),
-    "lmhead_gemm_kernel": ("lmhead.cu", "sv_device.cuh", "sv_draw.cuh", "sv_host.h"),
-    "cluster_kernel": ("cluster.cu", "sv_args.cuh", "sv_device.cuh", "sv_draw.cuh", "sv_host.h"),
+    "lmhead_gemm_kernel": ("lmhead.cu", "sv_device.cuh", "sv_draw.cuh", "sv_host.h", "sv_slice.cuh"),
+    "cluster_kernel": ("cluster.cu", "sv_args.cuh", "sv_device.cuh", "sv_draw.cuh", "sv_host.h", "sv_slice.cuh"),
 }
 KERNEL_SOURCES["fused_kernel_ragged"] = KERNEL_SOURCES["fused_kernel"]  # the same kernel, its ragged capture
 

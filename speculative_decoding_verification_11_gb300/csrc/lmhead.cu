@@ -34,6 +34,7 @@
 #include "sv_device.cuh"
 #include "sv_draw.cuh"
 #include "sv_host.h"
+#include "sv_slice.cuh"
 
 namespace sv {
 namespace lm {
@@ -680,55 +681,6 @@ __device__ __forceinline__ void fin_r(const float4 (&z)[2], const float4 (&qv)[2
         }
     }
 }
-__device__ __forceinline__ void fin_load_r(const float *zrow, const float *qrow, int V, int g, int lane, float c,
-                                           float M, float invS, float (&r)[2][4]) {
-    float4 z[2], qv[2];
-    fin_fetch(zrow, qrow, V, g, lane, z, qv);
-    fin_r(z, qv, qrow != nullptr, V, g, lane, c, M, invS, r);
-}
-
-// Sum of segment g's r over the whole row: this CTA's own segments from
-// shared memory, the others from the global scratch row (written before the
-// cluster barrier by the CTA that owns them).
-__device__ __forceinline__ float fin_seg_mass(const float *s_seg, const float *gseg, int g, int seg0, int seg1) {
-    return (g >= seg0 && g < seg1) ? s_seg[g - seg0] : __ldcg(gseg + g);
-}
-
-// First token with r > 0 at or after segment g0 (forward) or the last one at
-// or before it (backward); -1 if there is none.  Warp-wide; 32 segment sums
-// are examined per step.
-template <bool kForward>
-__device__ int fin_find_positive(const float *zrow, const float *qrow, int V, int ns, float c, float M, float invS,
-                                 const float *s_seg, const float *gseg, int seg0, int seg1, int g0, int lane,
-                                 float *rv) {
-    for (int base = g0; kForward ? base < ns : base >= 0; base += kForward ? 32 : -32) {
-        const int g = kForward ? base + lane : base - lane;
-        const bool has = (kForward ? g < ns : g >= 0) && fin_seg_mass(s_seg, gseg, g, seg0, seg1) > 0.f;
-        const unsigned m = __ballot_sync(0xffffffffu, has);
-        if (!m) continue;
-        const int gs = __shfl_sync(0xffffffffu, g, __ffs(m) - 1);
-        float r[2][4];
-        fin_load_r(zrow, qrow, V, gs, lane, c, M, invS, r);
-        int loc = kForward ? 0x7fffffff : -1;
-        float rloc = 0.f;
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int jj = kForward ? 1 - j : j, kk = kForward ? 3 - k : k;  // keep the extreme one
-                if (r[jj][kk] > 0.f) {
-                    loc = (jj * 32 + lane) * 4 + kk;
-                    rloc = r[jj][kk];
-                }
-            }
-        const int best = kForward ? __reduce_min_sync(0xffffffffu, loc) : __reduce_max_sync(0xffffffffu, loc);
-        if (kForward ? best == 0x7fffffff : best < 0) continue;  // a positive sum of nothing: cannot happen
-        const unsigned mm = __ballot_sync(0xffffffffu, loc == best);
-        *rv = __shfl_sync(0xffffffffu, rloc, __ffs(mm) - 1);
-        return gs * kSegElems + best;
-    }
-    return -1;
-}
 
 template <bool kSample>
 __global__ void __launch_bounds__(kFinThreads, 2) verify_finish_kernel(const float *spill, const float2 *partials,
@@ -955,18 +907,19 @@ __global__ void __launch_bounds__(kFinThreads, 2) verify_finish_kernel(const flo
             const int fseg = seg0 + __shfl_sync(0xffffffffu, found, src);
             const DS fbase = ds_shfl(fb, src);
             float r[2][4];
-            fin_load_r(zrow, qrow, V, fseg, lane, c, M, invS, r);
+            seg_r<float>(zrow + static_cast<size_t>(fseg) * kSegElems,
+                         qrow ? qrow + static_cast<size_t>(fseg) * kSegElems : nullptr, fseg, V, c, M, invS, lane, r);
             const TileScan ts = warp_seg_scan(r, fseg, V, fbase, t, lane);
             vstar = ts.v;
             rstar = ts.rv;
             next = fseg + 1;
         }
         if (vstar < 0)
-            vstar = fin_find_positive<true>(zrow, qrow, V, ns, c, M, invS, s_seg, gseg, seg0, seg1, next, lane,
+            vstar = find_positive<float, true>(zrow, qrow, V, ns, c, M, invS, s_seg, gseg, seg0, seg1, next, lane,
                                             &rstar);
     }
     if (vstar < 0)
-        vstar = fin_find_positive<false>(zrow, qrow, V, ns, c, M, invS, s_seg, gseg, seg0, seg1, ns - 1, lane,
+        vstar = find_positive<float, false>(zrow, qrow, V, ns, c, M, invS, s_seg, gseg, seg0, seg1, ns - 1, lane,
                                          &rstar);
     if (lane == 0) {
         out_tokens[r0 + ks] = vstar;
