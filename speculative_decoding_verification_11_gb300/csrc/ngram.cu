@@ -6,7 +6,7 @@
 // third page (prompt lookup matches strings already in the context).
 //
 // One CTA per request.  The context's last n_max tokens sit in shared memory,
-// and the context passes through shared memory in tiles of 4096 tokens (with
+// and the context passes through shared memory in tiles of 8192 tokens (with
 // the 32 tokens before each tile kept as a halo); every thread takes
 // candidate end positions e <= L - 2 and measures m(e),
 // the length of the common suffix of ctx[..e] and ctx[..L-1] (at most
@@ -22,9 +22,9 @@
 namespace sv {
 namespace ng {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kMaxN = 32;
-constexpr int kTile = 4096;            // context tokens staged in shared memory at a time
+constexpr int kTile = 8192;            // context tokens staged in shared memory at a time
 constexpr int kPerThread = kTile / kThreads;
 
 __global__ void __launch_bounds__(kThreads) ngram_kernel(const int32_t *tokens, const int32_t *ctx_offsets, int K,
