@@ -2,8 +2,8 @@
 
 TEST INFRASTRUCTURE ONLY (see oracle/__init__.py): plain Python per request.
 
-What it follows: the third page's "Dynamic speculative decoding" (the number
-of draft tokens is adapted; the metric is goodput = AL / ITL, with ITL the
+What it follows: "Hardware Aware Dynamic Speculative Decoding", section
+"Dynamic speculative decoding" (the number of draft tokens is adapted; the metric is goodput = AL / ITL, with ITL the
 inter-token latency, largely draft plus verify time; the optimal K is kept in
 a table that can take live AL and ITL statistics), and "Speculative Decoding
 in Production: Accelerating LLM Inference via Custom Draft Models",

@@ -6,9 +6,10 @@ request's token list, in the order the method is stated.
 What it follows: "Co-Designing AI Models Using Speculative Decoding for
 Faster LLM Inference", Table 1 (suffix / n-gram drafting: string matching over
 the token stream, no model, one lookup, best for workloads with high
-repetition), and the "Model-free methods" passage of the third page (n-gram
-or prompt-lookup drafting proposes tokens by matching strings that already
-appear in the context).
+repetition), and the model-free passage of "Speculative Decoding"
+(glossary), section "Variants: Draft Models, EAGLE, Medusa, and Model-Free
+Methods" (n-gram or prompt-lookup drafting proposes tokens by matching strings
+that already appear in the context).
 
 Readings (the pages give no algorithm):
   - for n = n_max down to n_min: the suffix is the context's last n tokens;

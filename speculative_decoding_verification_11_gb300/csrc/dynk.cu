@@ -1,6 +1,7 @@
 // Dynamic draft length (K) after verification, on the device: the accept
 // lengths never leave the GPU between a verification and the next step's
-// drafting.  The third page's "Dynamic speculative decoding" (K adapted to
+// drafting.  "Hardware Aware Dynamic Speculative Decoding", section "Dynamic
+// speculative decoding" (K adapted to
 // the hardware and the acceptance; goodput = AL / ITL, an offline table that
 // can take live AL and ITL statistics) and "Speculative Decoding in
 // Production: Accelerating LLM Inference via Custom Draft Models",

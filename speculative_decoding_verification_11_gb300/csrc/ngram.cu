@@ -2,8 +2,9 @@
 // followed the latest earlier occurrence of the context's longest matching
 // suffix.  "Co-Designing AI Models Using Speculative Decoding for Faster LLM
 // Inference", Table 1 (suffix / n-gram: string matching over the token
-// stream, no model, one lookup), and the "Model-free methods" passage of the
-// third page (prompt lookup matches strings already in the context).
+// stream, no model, one lookup), and the model-free passage of "Speculative
+// Decoding" (glossary), section "Variants: Draft Models, EAGLE, Medusa, and
+// Model-Free Methods" (prompt lookup matches strings already in the context).
 //
 // One CTA per request.  The context's last n_max tokens sit in shared memory,
 // and the context passes through shared memory in tiles of 8192 tokens (with
