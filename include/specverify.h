@@ -214,8 +214,9 @@ sv_status spec_ngram_draft(const int32_t *tokens, const int32_t *ctx_offsets, in
 
 /*
  * Dynamic draft length after verification ("Hardware Aware Dynamic
- * Speculative Decoding", section "Dynamic speculative decoding": K adapted to acceptance and hardware, goodput =
- * AL / ITL, a table extended with live statistics; "Speculative Decoding in
+ * Speculative Decoding", section "Dynamic speculative decoding": K adapted to
+ * acceptance and hardware, goodput = AL / ITL, a table extended with live
+ * statistics; "Speculative Decoding in
  * Production: Accelerating LLM Inference via Custom Draft Models", "Production
  * Failure Modes and Mitigation Strategies", item 1: K from 5 down to 1 or 2
  * when the average accepted length over the last 10 falls below 1.5).
