@@ -39,7 +39,7 @@ __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) {
 // Copy n elements of the request's rows into shared memory (16-byte vectors
 // when both ends allow, elements otherwise).  A thread issues up to kCopyBatch
 // loads before it stores any of them: one round trip instead of one per load.
-constexpr int kCopyBatch = 8;
+constexpr int kCopyBatch = 6;  // six loads per thread in flight keep 5 CTAs per SM resident (48 registers)
 template <typename T>
 __device__ __forceinline__ void load_rows(T *dst, const T *src, size_t n, int tid) {
     const size_t bytes = n * sizeof(T);
