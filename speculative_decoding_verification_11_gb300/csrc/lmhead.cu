@@ -71,6 +71,8 @@ template <int BN> struct LmSmem {
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort;
+    // each epilogue warp's 32 x 32 block of the logits copy, 128-byte swizzled, for a bulk tensor store
+    alignas(1024) float stage[kEpiWarps][32 * 32];
 };
 
 struct LmArgs {
@@ -78,6 +80,7 @@ struct LmArgs {
     float c;          // log2(e) / T
     float *spill;     // M x V fp32 logits (sampling), or nullptr
     int spill_keep;   // 1: the spill is read back from L2 soon (stores at evict_last priority)
+    int spill_tma;    // 1: the spill is written by bulk tensor stores through the third tensor map
     float2 *partials; // M x gridDim.x: one merged partial per row and CTA
     uint32_t *status;
 };
@@ -135,6 +138,20 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// Bulk tensor store of a box from shared memory, tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x, int y, uint64_t policy) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_addr(src)), "r"(x), "r"(y), "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The thread's committed bulk stores have read their shared memory / have completed.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Order this thread's generic-proxy shared-memory writes before later async-proxy reads of them.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
                  "r"(ncols)
@@ -186,7 +203,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 // ---------------------------------------------------------------------------
 template <bool kSample, int BN>
 __global__ void __launch_bounds__(kThreadsLm, 1)
-    lmhead_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, LmArgs a) {
+    lmhead_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmC, LmArgs a) {
     constexpr int kStagesLm = Tile<BN>::kStages;
     constexpr int kBBytes = Tile<BN>::kBBytes;
     constexpr int kTmemCols = Tile<BN>::kTmemCols;
@@ -282,6 +300,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
         const bool live = row < a.M;
         const bool vec_store = (a.V & 3) == 0;
         const uint64_t keep_pol = l2_evict_last_policy();
+        float *stage = sm.stage[quad];
         // running partial of this row over every tile of the CTA
         float Mr = -INFINITY, Sr = 0.f;
         float bv = -INFINITY;
@@ -300,7 +319,24 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                           v);
                 const int col0 = n0 + cb * 32;
                 const int nvalid = min(32, a.V - col0);
-                if (!live || nvalid <= 0) continue;
+                if (nvalid <= 0) continue;  // the same for the whole warp
+                if (kSample && a.spill_tma) {
+                    // the warp's 32 x 32 block of the copy: every lane stages its row (rows past M
+                    // and columns past V are clipped by the tensor map), one lane stores the box
+                    if (lane == 0) bulk_wait_read_all();  // the previous store has read the stage
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)  // 16-byte chunk j of row `lane`, 128-byte swizzle
+                        *reinterpret_cast<float4 *>(stage + lane * 32 + ((j ^ (lane & 7)) * 4)) =
+                            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, stage, col0, quad * 32, a.spill_keep ? keep_pol : l2_evict_normal_policy());
+                        bulk_commit();
+                    }
+                }
+                if (!live) continue;
                 if (kSample) {
                     float m = -INFINITY;
 #pragma unroll
@@ -316,7 +352,9 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                         Mr = Mn;
                     }
                     float *dst = a.spill + static_cast<size_t>(row) * a.V + col0;
-                    if (vec_store && nvalid == 32 && a.spill_keep) {
+                    if (a.spill_tma) {
+                        // stored above
+                    } else if (vec_store && nvalid == 32 && a.spill_keep) {
 #pragma unroll
                         for (int i = 0; i < 32; i += 4) st_f32x4_hint(dst + i, v[i], v[i + 1], v[i + 2], v[i + 3], keep_pol);
                     } else if (vec_store && nvalid == 32) {
@@ -341,6 +379,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.acc_empty[buf]);  // accumulator drained
         }
+        if (kSample && a.spill_tma && lane == 0) bulk_wait_all();  // the copy is complete before the kernel ends
         if (live)
             a.partials[static_cast<size_t>(row) * gridDim.x + blockIdx.x] =
                 kSample ? make_float2(Mr, Sr) : make_float2(bv, __int_as_float(bi));
@@ -380,6 +419,19 @@ static bool encode_bf16_kmajor(CUtensorMap *map, const void *base, int rows, int
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The M x V fp32 logits copy as 32 x 32 boxes, 128-byte swizzled (rows of V floats, V a multiple of 4).
+static bool encode_f32_rows(CUtensorMap *map, const float *base, int rows, int cols) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -427,27 +479,29 @@ static LmLayout lm_layout(int B, int K, int V) {
 
 // Launch with `grid` CTAs (grid <= n_tiles, <= kMaxLmGrid).
 template <bool kSample, int BN>
-static void launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const LmArgs &a, int grid, cudaStream_t s) {
+static void launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const LmArgs &a, int grid,
+                        cudaStream_t s) {
     static bool configured[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
+    static_assert(sizeof(LmSmem<BN>) + 1024 <= 232448, "shared memory of one CTA on this GPU");
     const int smem = static_cast<int>(sizeof(LmSmem<BN>)) + 1024;
     if (!configured[dev]) {
         cudaFuncSetAttribute(lmhead_gemm_kernel<kSample, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         configured[dev] = true;
     }
-    lmhead_gemm_kernel<kSample, BN><<<grid, kThreadsLm, smem, s>>>(ta, tb, a);
+    lmhead_gemm_kernel<kSample, BN><<<grid, kThreadsLm, smem, s>>>(ta, tb, tc, a);
 }
 
 template <bool kSample>
-static void launch_gemm_bn(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const LmArgs &a, int grid,
-                           cudaStream_t s) {
+static void launch_gemm_bn(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc, const LmArgs &a,
+                           int grid, cudaStream_t s) {
     switch (bn) {
-        case 224: launch_gemm<kSample, 224>(ta, tb, a, grid, s); break;
-        case 192: launch_gemm<kSample, 192>(ta, tb, a, grid, s); break;
-        case 128: launch_gemm<kSample, 128>(ta, tb, a, grid, s); break;
-        default: launch_gemm<kSample, 256>(ta, tb, a, grid, s); break;
+        case 224: launch_gemm<kSample, 224>(ta, tb, tc, a, grid, s); break;
+        case 192: launch_gemm<kSample, 192>(ta, tb, tc, a, grid, s); break;
+        case 128: launch_gemm<kSample, 128>(ta, tb, tc, a, grid, s); break;
+        default: launch_gemm<kSample, 256>(ta, tb, tc, a, grid, s); break;
     }
 }
 
@@ -984,10 +1038,13 @@ extern "C" sv_status spec_lmhead_verify(const void *hidden, const void *w_vocab_
     const bool cluster_finish = V % 4 == 0 && lm::fin_segs_per_cta(V) <= lm::kFinMaxSegs &&
                                 (!sample || K == 0 || (reinterpret_cast<uintptr_t>(q) & 15u) == 0);
     a.spill_keep = (sample && cluster_finish) ? 1 : 0;
+    // the copy through bulk tensor stores (rows of V floats must be 16-byte multiples)
+    CUtensorMap tc = tb;
+    a.spill_tma = (sample && V % 4 == 0 && lm::encode_f32_rows(&tc, a.spill, M, V)) ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     prof_begin(s);
-    if (sample) lm::launch_gemm_bn<true>(bn, ta, tb, a, grid, s);
-    else lm::launch_gemm_bn<false>(bn, ta, tb, a, grid, s);
+    if (sample) lm::launch_gemm_bn<true>(bn, ta, tb, tc, a, grid, s);
+    else lm::launch_gemm_bn<false>(bn, ta, tb, tc, a, grid, s);
     prof_end(s);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
     if (cluster_finish) {
@@ -1068,12 +1125,14 @@ extern "C" sv_status spec_draft_sample(const void *hidden, const void *w_vocab_t
     a.c = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(temperature)) : 1.f;
     a.spill = sample ? q_out : nullptr;  // the logits land in q's buffer, turned into q in place
     a.spill_keep = 1;                    // read back and rewritten as q by the finish kernel, from L2
+    CUtensorMap tc = tb;
+    a.spill_tma = (sample && lm::encode_f32_rows(&tc, a.spill, M, V)) ? 1 : 0;  // V % 4 == 0 here
     a.partials = reinterpret_cast<float2 *>(w + 256);
     a.status = reinterpret_cast<uint32_t *>(w);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     prof_begin(s);
-    if (sample) lm::launch_gemm_bn<true>(bn, ta, tb, a, grid, s);
-    else lm::launch_gemm_bn<false>(bn, ta, tb, a, grid, s);
+    if (sample) lm::launch_gemm_bn<true>(bn, ta, tb, tc, a, grid, s);
+    else lm::launch_gemm_bn<false>(bn, ta, tb, tc, a, grid, s);
     prof_end(s);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
