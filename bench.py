@@ -49,6 +49,8 @@ KERNEL_SOURCES = {
     "cluster_kernel": ("cluster.cu", "sv_args.cuh", "sv_device.cuh", "sv_draw.cuh", "sv_host.h", "sv_slice.cuh"),
 }
 KERNEL_SOURCES["fused_kernel_ragged"] = KERNEL_SOURCES["fused_kernel"]  # the same kernel, its ragged capture
+KERNEL_SOURCES["lmhead_gemm_kernel_draft"] = KERNEL_SOURCES["lmhead_gemm_kernel"]  # the draft head's capture
+KERNEL_SOURCES["ngram_kernel"] = ("ngram.cu", "sv_device.cuh", "sv_host.h")
 
 
 def _source_hash(kernel: str):
@@ -856,7 +858,8 @@ def run_draft(args):
                    "l2": "inputs 525 MB > L2, no flush"},
         "roofline": {"kernel": "lmhead_gemm_kernel (draft head)", "bound": "hbm",
                      "achieved": gemm_bytes / (gms * 1e-3) / 1e9, "peak": peak, "peak_kind": peak_kind,
-                     "unit": "GB/s", "frac": gemm_bytes / (gms * 1e-3) / 1e9 / peak, "traffic": None,
+                     "unit": "GB/s", "frac": gemm_bytes / (gms * 1e-3) / 1e9 / peak,
+                     "traffic": _traffic("lmhead_gemm_kernel_draft"),
                      "algorithmic_bytes_per_launch": gemm_bytes, "ms_per_launch": gms,
                      "tensor": {"achieved_tflops": flops / (gms * 1e-3) / 1e12, "peak_tflops": tpk,
                                 "peak_kind": tpk_kind, "frac": flops / (gms * 1e-3) / 1e12 / tpk}},
@@ -940,7 +943,7 @@ def run_ngram(args):
                           if args.l2_flush else
                           "contexts < L2: calls rotate over copies > 2 x L2, replayed back to back from a CUDA graph")},
         "roofline": {"kernel": "ng::ngram_kernel", "bound": "hbm", "achieved": head["achieved_gbs"], "peak": peak,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": head["achieved_gbs"] / peak, "traffic": None,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": head["achieved_gbs"] / peak, "traffic": _traffic("ngram_kernel"),
                      "algorithmic_bytes_per_launch": head["algorithmic_bytes"],
                      "ms_per_launch": head["us_per_call"] * 1e-3},
         "lengths": res, "gpu_launches": 2 * args.steps,
