@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("policy", [dynk.WINDOW, dynk.GOODPUT])
-@pytest.mark.parametrize("B,Wn", [(37, 10), (2500, 4)])
+@pytest.mark.parametrize("B,Wn", [(37, 10), (2500, 4), (4096, 10)])
 def test_controller_matches_oracle_over_steps(cuda_device, policy, B, Wn):
     dev = cuda_device
     rng = np.random.default_rng(B * 10 + policy)

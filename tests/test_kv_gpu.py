@@ -35,7 +35,7 @@ def _run(dev, bt, seq, free, fc, K, al, bs):
 
 
 @pytest.mark.parametrize("B,max_blocks,bs,kmax", [(64, 40, 16, 8), (7, 9, 1, 6), (300, 12, 3, 20),
-                                                  (2500, 6, 32, 64)])
+                                                  (2500, 6, 32, 64), (4096, 264, 16, 4)])
 def test_reserve_and_rollback_match_oracle(cuda_device, B, max_blocks, bs, kmax):
     rng = np.random.default_rng(B + bs)
     bt, seq, free, fc = _state(rng, B, max_blocks, bs, fill=0.55)

@@ -49,6 +49,17 @@ def test_repetitive_streams_workload(cuda_device):
     assert (k > 0).mean() > 0.5  # the streams repeat: most requests find a match
 
 
+@pytest.mark.parametrize("L", [8192, 32768])
+def test_timed_workload_at_full_size(cuda_device, L):
+    """The timed drafting workload at its own sizes (B = 256 contexts of L
+    tokens, K = 8, n = 1..4): every request against the oracle."""
+    tokens, offs = W.repetitive_streams(seed=1006, B=256, L=L)
+    d, k = _gpu(cuda_device, tokens, offs, 8, 1, 4)
+    od, ok = _oracle(tokens, offs, 8, 1, 4)
+    assert np.array_equal(k, ok) and np.array_equal(d, od)
+    assert 0 < (k > 0).mean() < 1  # both outcomes occur
+
+
 def test_decreasing_offsets_propose_nothing(cuda_device):
     tokens = np.array([1, 2, 1, 2, 1, 2], dtype=np.int32)
     d, k = _gpu(cuda_device, tokens, [0, 6, 2], 3, 1, 2)

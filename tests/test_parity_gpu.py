@@ -359,6 +359,52 @@ def test_one_workspace_serves_calls_of_any_shape(cuda_device):
             assert torch.equal(o1, o2) and torch.equal(a1, a2), (rep, b.B, b.K, b.V)
 
 
+def test_graph_replay_over_rotating_inputs(cuda_device, kernel):
+    """Calls captured in one CUDA graph, as the small workloads are timed:
+    sampling and greedy calls over different inputs, back to back on one
+    workspace.  Two replays give the oracle's results for every call."""
+    dev = cuda_device
+    samp = [_rand_batch(700 + i, B=12, K=3, V=9000, dtype=torch.float32, T=1.0) for i in range(3)]
+    gre = [_rand_batch(710 + i, B=12, K=3, V=9000, dtype=torch.bfloat16, T=0.0) for i in range(2)]
+    order = [samp[0], gre[0], samp[1], samp[2], gre[1]]
+    ws = B_.workspace(max(B_.spec_verify_workspace_size(b.B, b.rows, b.V) for b in order), dev)
+    ins = [(b.logits.to(dev), b.q.to(dev) if b.q is not None else None, b.draft.to(dev),
+            b.uniforms.to(dev) if b.uniforms is not None else None) for b in order]
+    outs = [(torch.empty(b.rows, dtype=torch.int32, device=dev), torch.empty(b.B, dtype=torch.int32, device=dev))
+            for b in order]
+
+    def calls(st):
+        for b, (lg, q, x, u), (o, a) in zip(order, ins, outs):
+            if b.temperature == 0:
+                B_.spec_verify_greedy(lg, x, b.B, b.K, b.V, o, a, ws, stream=st)
+            else:
+                B_.spec_verify_sample(lg, q, b.B, b.K, b.V, b.temperature, x, u, o, a, ws, stream=st)
+
+    stream = torch.cuda.current_stream(dev)
+    calls(stream)  # eager first: the same kernels, and the workspace's state carried into the graph
+    torch.cuda.synchronize()
+    gs = torch.cuda.Stream(dev)
+    gs.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=gs):
+        calls(gs)
+    orcs = [_oracle(b) for b in order]
+    for rep in range(2):
+        for o, a in outs:
+            o.fill_(-5)
+            a.fill_(-5)
+        g.replay()
+        torch.cuda.synchronize()
+        for i, (b, (o, a), orc) in enumerate(zip(order, outs, orcs)):
+            name = f"graph replay {rep} call {i} {kernel}"
+            if b.temperature == 0:
+                compare_greedy(name, b.row_offsets, o.cpu().numpy(), a.cpu().numpy(), orc)
+            else:
+                compare_sampling(name, b.row_offsets, o.cpu().numpy(), a.cpu().numpy(), None, orc)
+    st, flags = B_.spec_verify_last_device_status(ws)
+    assert st == B_.SV_OK and flags & ~B_.SV_FLAG_ZERO_RESIDUAL == 0
+
+
 def test_kernel_choice_follows_the_knobs(cuda_device):
     """The path a call takes, as spec_last_kernel() reports it, follows the
     size rules and the two process-wide knobs; every path gives the oracle's
