@@ -405,6 +405,55 @@ def test_graph_replay_over_rotating_inputs(cuda_device, kernel):
     assert st == B_.SV_OK and flags & ~B_.SV_FLAG_ZERO_RESIDUAL == 0
 
 
+def test_more_than_2_32_logits_with_planted_maxima(cuda_device):
+    """16 bf16 rows of V = 2^28 + 8 logits (4.3e9 elements, past 2^32) and 12
+    fp32 q rows (3.2e9 elements, past 2^31), so that every row, gather and
+    residual offset past the first rows needs 64-bit indexing.  Each row is 0
+    except a planted +100 at t_r, so p is one-hot at t_r in fp32 (the other
+    tokens get e^-100 / S < 4e-44) and the results follow by construction:
+    drafts equal to t_j with q one-hot there are accepted; a draft elsewhere
+    with q one-hot at it is rejected, and its residual max(0, p - q) is
+    one-hot at t_j again.  So request b emits t_0 .. t_{a_b} and AL = a_b + 1,
+    where a_b is the first position whose draft misses.  Greedy verification
+    of the same logits gives the same result."""
+    dev = cuda_device
+    B, K, V = 4, 3, (1 << 28) + 8
+    R, Nq = B * (K + 1), B * K
+    miss = [0, 1, 2, K]  # first drafted position that misses t; K: every draft matches (bonus)
+    t = [(V - 1 - 1009 * r) if r % 2 else (1000003 * r + 4099) % V for r in range(R)]
+    x = []
+    for b in range(B):
+        for j in range(K):
+            tj = t[b * (K + 1) + j]
+            x.append(tj if j < miss[b] else (tj + 12345) % V)
+    logits = torch.zeros(R, V, dtype=torch.bfloat16, device=dev)
+    logits[torch.arange(R, device=dev), torch.tensor(t, device=dev)] = 100.0
+    q = torch.zeros(Nq, V, dtype=torch.float32, device=dev)
+    q[torch.arange(Nq, device=dev), torch.tensor(x, device=dev)] = 1.0
+    draft = torch.tensor(x, dtype=torch.int32, device=dev)
+    u = torch.from_numpy(W.philox_uniforms(4321, R)).to(dev)
+    exp_out = np.full(R, -1, dtype=np.int32)
+    for b in range(B):
+        exp_out[b * (K + 1):b * (K + 1) + miss[b] + 1] = t[b * (K + 1):b * (K + 1) + miss[b] + 1]
+    exp_al = np.array(miss, dtype=np.int32) + 1
+    ws = B_.workspace(B_.spec_verify_workspace_size(B, R, V), dev)
+    out = torch.full((R,), -9, dtype=torch.int32, device=dev)
+    al = torch.full((B,), -9, dtype=torch.int32, device=dev)
+    B_.spec_verify_sample(logits, q, B, K, V, 1.0, draft, u, out, al, ws)
+    torch.cuda.synchronize()
+    assert B_.spec_last_kernel() == "stream"
+    assert np.array_equal(al.cpu().numpy(), exp_al) and np.array_equal(out.cpu().numpy(), exp_out)
+    out.fill_(-9)
+    al.fill_(-9)
+    B_.spec_verify_greedy(logits, draft, B, K, V, out, al, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(al.cpu().numpy(), exp_al) and np.array_equal(out.cpu().numpy(), exp_out)
+    st, flags = B_.spec_verify_last_device_status(ws)
+    assert st == B_.SV_OK and flags == 0
+    del logits, q
+    torch.cuda.empty_cache()
+
+
 def test_kernel_choice_follows_the_knobs(cuda_device):
     """The path a call takes, as spec_last_kernel() reports it, follows the
     size rules and the two process-wide knobs; every path gives the oracle's
