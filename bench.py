@@ -726,6 +726,8 @@ def run_kv(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     res = {}
+    clocks = Clocks(0)
+    clocks.start()
     for Bn in (64, 4096):
         rng = np.random.default_rng(7 + Bn)
         bs, K, max_blocks = 16, 4, 264
@@ -778,6 +780,7 @@ def run_kv(args):
         alg = Bn * 4 * 5 + new_blocks * 4 * 6
         res[f"B={Bn}"] = {"us_per_step": ms * 1e3, "blocks_moved_per_step": 2 * new_blocks,
                           "algorithmic_bytes": alg, "achieved_gbs": alg / (ms * 1e-3) / 1e9}
+    clk = clocks.stop()
     peak, peak_kind = _peaks()
     head = res["B=64"]
     line = {
@@ -793,7 +796,7 @@ def run_kv(args):
                      "algorithmic_bytes_per_launch": head["algorithmic_bytes"] / 2,
                      "ms_per_launch": head["us_per_step"] * 1e-3 / 2,
                      "note": "latency-bound: one CTA and two dependent launches per step"},
-        "batches": res, "gpu_launches": 2 * args.steps,
+        "batches": res, "clocks": clk, "gpu_launches": 2 * args.steps,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -886,6 +889,8 @@ def run_ngram(args):
     fr = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if args.l2_flush else None
     res = {}
     B, K, n_min, n_max = 256, 8, 1, 4
+    clocks = Clocks(0)
+    clocks.start()
     for L in (8192, 32768):
         tokens, offs = W.repetitive_streams(seed=1006, B=B, L=L)
         t = torch.from_numpy(tokens).to(dev)
@@ -932,6 +937,7 @@ def run_ngram(args):
         res[f"L={L}"] = {"us_per_call": ms * 1e3, "requests_per_s": B / (ms * 1e-3),
                          "mean_draft_len": float(kh.float().mean()), "with_proposal": float((kh > 0).float().mean()),
                          "algorithmic_bytes": alg, "achieved_gbs": alg / (ms * 1e-3) / 1e9}
+    clk = clocks.stop()
     peak, peak_kind = _peaks()
     head = res["L=8192"]
     line = {
@@ -946,7 +952,7 @@ def run_ngram(args):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": head["achieved_gbs"] / peak, "traffic": _traffic("ngram_kernel"),
                      "algorithmic_bytes_per_launch": head["algorithmic_bytes"],
                      "ms_per_launch": head["us_per_call"] * 1e-3},
-        "lengths": res, "gpu_launches": 2 * args.steps,
+        "lengths": res, "clocks": clk, "gpu_launches": 2 * args.steps,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -963,6 +969,8 @@ def run_dynk(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     res = {}
+    clocks = Clocks(0)
+    clocks.start()
     for Bn in (64, 4096):
         g = torch.Generator().manual_seed(Bn)
         al = torch.randint(1, 6, (Bn,), generator=g, dtype=torch.int32).to(dev)
@@ -994,6 +1002,7 @@ def run_dynk(args):
         alg = Bn * (4 * 4 + 10 * 8 + 8) + 9 * 4  # AL, K used, count, k_next; the ring read (and one pair written); offsets
         res[f"B={Bn}"] = {"us_per_update": us, "algorithmic_bytes": alg, "achieved_gbs": alg / (us * 1e-6) / 1e9,
                           "mean_k_next": float(kn.float().mean())}
+    clk = clocks.stop()
     peak, peak_kind = _peaks()
     head = res["B=64"]
     line = {
@@ -1007,7 +1016,7 @@ def run_dynk(args):
                      "algorithmic_bytes_per_launch": head["algorithmic_bytes"],
                      "ms_per_launch": head["us_per_update"] * 1e-3,
                      "note": "latency-bound: one CTA per update, in a CUDA graph"},
-        "batches": res, "gpu_launches": args.steps,
+        "batches": res, "clocks": clk, "gpu_launches": args.steps,
     }
     print(json.dumps(line), flush=True)
     return 0

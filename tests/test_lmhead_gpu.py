@@ -123,6 +123,25 @@ def test_lmhead_vocab_not_multiple_of_4(cuda_device):
     _compare("lmhead B=5 K=3 d=512 V=4001 T=0.9", b, 0.9, cuda_device)
 
 
+@pytest.fixture(scope="module")
+def wide_batch():
+    return W.lmhead(seed=3315, B=4, K=3, d=256, V=300000, d_draft=256, T=1.0)
+
+
+def test_lmhead_vocab_past_the_cluster_finish(cuda_device, wide_batch):
+    """V = 300000 is past the largest vocabulary the one-cluster-per-request
+    finish takes (8 CTAs x 96 segments x 256 tokens = 196608): the GEMM runs
+    ~9 tiles per CTA and the call finishes with the decide and residual
+    kernels over the logits copy (three launches in all)."""
+    _compare("lmhead wide B=4 K=3 d=256 V=300000 T=1", wide_batch, 1.0, cuda_device)
+    assert B_.spec_last_launch_count() == 3
+
+
+def test_lmhead_vocab_past_the_cluster_finish_greedy(cuda_device, wide_batch):
+    _compare("lmhead wide greedy B=4 K=3 d=256 V=300000", wide_batch, 0.0, cuda_device)
+    assert B_.spec_last_launch_count() == 2
+
+
 def test_lmhead_zero_residual_falls_back_to_p(cuda_device):
     """q >= p everywhere: every residual is empty, so the token is drawn from
     p and the call flags it."""
