@@ -50,6 +50,23 @@ def test_uniform_mapping_and_the_input_generator_agree():
     assert np.array_equal(got.astype(np.float32).astype(np.float64), got)  # exact in fp32
 
 
+def test_draft_uniforms_follow_their_counters():
+    """Draw r of a call with counter offset o uses Philox counter (o + r,
+    stream 1): the uniforms draft_sample reports equal the input generator's
+    (numpy, written separately) for that stream and offset, and another offset
+    gives other uniforms."""
+    g = torch.Generator().manual_seed(17)
+    M, d, V = 6, 64, 300
+    h = torch.randn(M, d, generator=g).to(torch.bfloat16)
+    w = (torch.randn(V, d, generator=g) * 0.1).to(torch.bfloat16)
+    seed = 0xABCDEF012345
+    for offset in (0, 777, 2**33 + 5):
+        got = D.draft_sample(h, w, 1.0, seed, offset)["u"]
+        ref = W.philox_uniforms(seed, M, stream=1, offset=offset).astype(np.float64)
+        assert np.array_equal(got, ref), offset
+    assert not np.array_equal(D.draft_sample(h, w, 1.0, seed, 0)["u"], D.draft_sample(h, w, 1.0, seed, 1)["u"])
+
+
 def test_draw_matches_exact_rational_enumeration():
     rng = np.random.default_rng(3)
     for _ in range(300):

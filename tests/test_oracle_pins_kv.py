@@ -162,3 +162,26 @@ def test_out_of_blocks_and_bad_inputs_change_nothing():
     hole = np.array([[1, -1], [2, -1]], dtype=np.int32)      # a block to free is missing
     r = kv.rollback(hole, seq, free, 1, np.array([3, 0]), np.array([1, 1]), bs)
     assert r[4] == kv.BAD_INPUT
+
+
+def test_exactly_enough_free_blocks():
+    """The free list holding exactly the blocks a reservation needs is enough
+    (the stack empties); one block fewer is not.  The rollback that follows
+    fills the stack back to its capacity, and one slot less of capacity is
+    refused."""
+    bs = 4
+    bt = np.array([[1, -1, -1], [2, -1, -1]], dtype=np.int32)
+    seq = np.array([4, 3], dtype=np.int32)
+    free = np.array([7, 5, 6], dtype=np.int32)
+    # request 0 needs blocks 1 and 2 (4 + 6 tokens), request 1 block 1 (3 + 3): 3 blocks, 3 free
+    bt1, fc1, st = kv.reserve(bt, seq, free, 3, np.array([6, 3]), bs)
+    assert st == kv.OK and fc1 == 0
+    assert list(bt1[0]) == [1, 7, 5] and list(bt1[1]) == [2, 6, -1]
+    out = kv.reserve(bt, seq, free[:2], 2, np.array([6, 3]), bs)
+    assert out[2] == kv.OUT_OF_BLOCKS and np.array_equal(out[0], bt) and out[1] == 2
+    bt2, seq2, free2, fc2, st = kv.rollback(bt1, seq, free, fc1, np.array([6, 3]), np.array([1, 1]), bs)
+    assert st == kv.OK and fc2 == 3 and list(free2) == [7, 5, 6]
+    assert np.array_equal(bt2, bt) and np.array_equal(seq2, seq)
+    r = kv.rollback(bt1, seq, free[:2], fc1, np.array([6, 3]), np.array([1, 1]), bs)
+    assert r[4] == kv.BAD_INPUT and np.array_equal(r[0], bt1)
+
