@@ -191,17 +191,16 @@ def argmax_rows(z) -> np.ndarray:
                      for r in range(rows)], dtype=np.int64)
 
 
-def lmhead_logits(hidden, w_vocab_t, rows=None, v_chunk: int = 8192) -> np.ndarray:
+def lmhead_logits(hidden, w_vocab_t, v_chunk: int = 8192) -> np.ndarray:
     """z = hidden . W_vocab in fp64 from the bf16-decoded operands.
 
     hidden (M, d) bf16; w_vocab_t (V, d) bf16, i.e. W_vocab stored transposed
-    (row v holds the d weights of vocabulary entry v).  ``rows`` selects a
-    subset of hidden rows.  The product is a library matmul in fp64, taken in
+    (row v holds the d weights of vocabulary entry v).  The product is a
+    library matmul in fp64, taken in
     column blocks of the vocabulary to bound host memory.
     """
     import torch
-    h = hidden if rows is None else hidden[rows]
-    h64 = h.to(torch.float64).numpy()
+    h64 = hidden.to(torch.float64).numpy()
     V = w_vocab_t.shape[0]
     out = np.empty((h64.shape[0], V), dtype=np.float64)
     for v0 in range(0, V, v_chunk):

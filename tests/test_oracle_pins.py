@@ -436,3 +436,125 @@ def test_expected_tokens_limits():
     # page 1's speedup reduces to AL when verification of B(1+D) costs the
     # same as of B and drafting is free
     assert speedup.measured_speedup(2.0, 2.0, 0.0, 3.7) == pytest.approx(3.7)
+
+
+# --------------------------------------------------------------------------
+# batch layout, input rules and the draw's edges
+# --------------------------------------------------------------------------
+def _ragged_case(seed, ks, V, dtype=np.float32):
+    rng = np.random.default_rng(seed)
+    ro = np.concatenate([[0], np.cumsum(np.asarray(ks) + 1)]).astype(np.int32)
+    R, nq = int(ro[-1]), int(ro[-1]) - len(ks)
+    z = rng.normal(0, 2.0, size=(R, V)).astype(dtype)
+    zq = rng.normal(0, 2.0, size=(nq, V))
+    q = (np.exp(zq) / np.exp(zq).sum(1, keepdims=True)).astype(np.float32)
+    x = np.array([rng.choice(V, p=q[i].astype(np.float64) / q[i].astype(np.float64).sum()) for i in range(nq)],
+                 dtype=np.int32)
+    u = rng.uniform(0.001, 0.999, size=R).astype(np.float32)
+    return z, q, x, u, ro
+
+
+@pytest.mark.parametrize("greedy", [False, True])
+def test_ragged_batch_equals_its_requests_one_by_one(greedy):
+    """Request b of a CSR batch owns logits rows, uniforms and output slots
+    ro[b] .. ro[b+1]-1 and q rows / draft ids ro[b]-b .. ro[b+1]-b-2: the batch
+    gives what each request gives alone."""
+    ks = [3, 0, 5, 1, 0, 2, 4]
+    z, q, x, u, ro = _ragged_case(5, ks, 40)
+    res = oracle.verify(z, q, x, u, ro, 0.9, greedy=greedy)
+    for b, k in enumerate(ks):
+        r0, d0 = int(ro[b]), int(ro[b]) - b
+        one = oracle.verify_fixed(z[r0:r0 + k + 1], q[d0:d0 + k], x[d0:d0 + k], u[r0:r0 + k + 1], 1, k, 0.9,
+                                  greedy=greedy)
+        assert res["accept_len"][b] == one["accept_len"][0], b
+        assert np.array_equal(res["out_tokens"][r0:r0 + k + 1], one["out_tokens"]), b
+
+
+def test_malformed_offsets_are_refused():
+    z = np.zeros((5, 8), np.float32)
+    q = np.full((3, 8), 0.125, np.float32)
+    x = np.zeros(3, np.int32)
+    u = np.full(5, 0.5, np.float32)
+    for ro in ([0, 3, 3, 5], [0, 4, 3, 5], [1, 3, 5]):  # an empty request, decreasing, not from 0
+        with pytest.raises(ValueError):
+            oracle.verify(z, q, x, u, np.array(ro, np.int32), 1.0)
+
+
+def test_drafted_id_equal_to_vocab_size_is_invalid():
+    V = 6
+    z = np.zeros((3, V), np.float32)
+    q = np.full((2, V), 1.0 / V, np.float32)
+    u = np.full(3, 0.5, np.float32)
+    res = oracle.verify_fixed(z, q, np.array([0, V], np.int32), u, 1, 2, 1.0)
+    assert res["invalid"] == 1 and res["accept_len"][0] == 0 and list(res["out_tokens"]) == [-1, -1, -1]
+    res = oracle.verify_fixed(z, q, np.array([0, V - 1], np.int32), u, 1, 2, 1.0)
+    assert res["invalid"] == 0 and res["accept_len"][0] >= 1
+
+
+def test_draw_with_no_boundary_above_u_takes_the_last_positive_token():
+    """The reading for a draw that rounding leaves without a boundary above
+    u R: the largest token with r > 0.  A final uniform of exactly 1 makes
+    that happen (u R = R = C(V-1)); the tokens after the last positive one
+    have z = -inf, so p and r are 0 there."""
+    z = np.array([[0.3, -1.0, 2.0, 0.0, 1.5, -0.5, 0.7, -np.inf, -np.inf, -np.inf]])
+    res = oracle.verify_fixed(z, np.zeros((0, 10), np.float32), np.zeros(0, np.int32),
+                              np.array([1.0], np.float32), 1, 0, 1.0)
+    assert res["out_tokens"][0] == 6 and res["near_tie_sample"][0] == 1
+
+
+def test_accept_near_tie_is_measured_on_p_over_q():
+    """p(x) = 1/4 (four equal logits), q(x) = 1/2: the accept threshold p/q is
+    1/2.  A uniform 6e-8 above it is a near tie; one at 0.6 is not."""
+    z = np.zeros((2, 4))
+    q = np.array([[0.5, 0.5 / 3, 0.5 / 3, 0.5 / 3]], np.float32)
+    u_near = np.nextafter(np.float32(0.5), np.float32(1.0))
+    for u0, tie in ((u_near, 1), (np.float32(0.6), 0)):
+        res = oracle.verify_fixed(z, q, np.array([0], np.int32), np.array([u0, 0.3], np.float32), 1, 1, 1.0)
+        assert res["near_tie_accept"][0] == tie, u0
+        assert res["accept_len"][0] == 1  # u > 1/2: rejected either way
+
+
+def test_zero_residual_draws_from_p_not_uniformly():
+    """q = 1 everywhere leaves an empty residual after every rejection; the
+    token is the inverse-CDF draw from the (non-uniform) p with the final
+    uniform, computed here with numpy from the page's softmax."""
+    rng = np.random.default_rng(11)
+    B, V = 40, 64
+    z = rng.normal(0, 2.0, size=(2 * B, V))
+    q = np.ones((B, V), np.float32)
+    x = rng.integers(0, V, size=B).astype(np.int32)
+    u = rng.uniform(0.01, 0.99, size=2 * B).astype(np.float32)
+    res = oracle.verify_fixed(z, q, x, u, B, 1, 1.0)
+    checked = 0
+    for b in range(B):
+        assert res["accept_len"][b] == 1 and res["zero_residual"][b] == 1
+        p = np.exp(z[2 * b] - z[2 * b].max())
+        c = np.cumsum(p) / p.sum()
+        uf = float(u[2 * b + 1])
+        if np.min(np.abs(c - uf)) < 1e-9:
+            continue
+        assert res["out_tokens"][2 * b] == int(np.searchsorted(c, uf, side="right")), b
+        checked += 1
+    assert checked >= B - 2
+
+
+def test_results_do_not_change_when_every_logit_is_shifted():
+    """softmax(z + c) = softmax(z): fp64 logits shifted by 1000 (exp(1000)
+    overflows fp64 without the max subtraction) give the same results."""
+    z, q, x, u, ro = _ragged_case(9, [2, 3, 0, 1], 30, dtype=np.float64)
+    a = oracle.verify(z, q, x, u, ro, 0.8)
+    b = oracle.verify(z + 1000.0, q, x, u, ro, 0.8)
+    assert np.array_equal(a["accept_len"], b["accept_len"]) and np.array_equal(a["out_tokens"], b["out_tokens"])
+    assert np.allclose(a["p_draft"], b["p_draft"], rtol=1e-9, atol=0, equal_nan=True)
+    assert np.allclose(oracle.softmax_rows(z + 1000.0, 0.8), oracle.softmax_rows(z, 0.8), rtol=1e-9, atol=1e-300)
+
+
+@pytest.mark.parametrize("alpha,gamma,c", [(0.6, 4, 0.05), (0.8, 7, 0.1), (0.3, 2, 0.02)])
+def test_measured_speedup_reduces_to_the_cycle_model(alpha, gamma, c):
+    """With the cycle model's costs (one target call of unit time at either
+    batch size, as the memory-bound verification makes it, gamma draft steps
+    of c each) and AL = E[N], the measured-times formula of "Co-Designing AI
+    Models..." equals the closed form of "Speculative Decoding in Large
+    Language Models", section 2."""
+    got = speedup.measured_speedup(1.0, 1.0, gamma * c, speedup.expected_tokens(alpha, gamma))
+    assert abs(got - speedup.cycle_speedup(alpha, gamma, c)) < 1e-12
