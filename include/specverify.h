@@ -116,7 +116,9 @@ sv_status spec_verify_greedy(const void *logits, sv_dtype dt, int B, int K, int 
 /*
  * Sampling verification ("Speculative Decoding in Large Language Models",
  * section 2 "Modified Rejection Sampling"; the glossary's "Mathematical
- * Guarantee"; page-4 equations for alpha and P').
+ * Guarantee"; "Speculative Decoding in Production: Accelerating LLM
+ * Inference via Custom Draft Models", "Speculative Decoding Mechanics", the
+ * equations for alpha and P').
  *   logits      (B (K+1)) x V, dtype dt;   q  (B K) x V fp32 (already tempered)
  *   temperature T > 0;  draft B K int32;  uniforms B (K+1) fp32 in (0, 1)
  *   out_tokens  B (K+1) int32;  accept_len B int32;  diag see above
@@ -155,11 +157,22 @@ size_t spec_lmhead_workspace_size(int B, int K, int d, int V);
  * product z = hidden . W_vocab (bf16 operands, fp32 accumulation on the
  * tensor cores) and feed the verifier tile by tile; this is the GEMM whose M
  * grows from B to B (1 + D) under speculation ("Co-Designing...", Guideline 1).
- *   hidden     M x d bf16, M = B (K+1) <= 128, d a multiple of 64
- *   w_vocab_t  V x d bf16: W_vocab stored transposed (row v = the d weights
- *              of token v, the layout of a Linear layer's weight); V % 16 == 0
+ *   hidden     M x d bf16, row-major, 16-byte aligned; M = B (K+1) <= 128,
+ *              d a multiple of 64
+ *   w_vocab_t  V x d bf16, 16-byte aligned: W_vocab stored transposed (row
+ *              v = the d weights of token v, the layout of a Linear layer's
+ *              weight); any V >= 1
  *   q, draft, uniforms, out_tokens, accept_len, diag as in spec_verify_sample
  *   temperature 0 = greedy, else sampling
+ *   ws         spec_lmhead_workspace_size(B, K, d, V) bytes, 256-byte aligned
+ * Two launches when V is a multiple of 4, V <= 196608 and q (if used) is
+ * 16-byte aligned: the GEMM, then one cluster of CTAs per request that
+ * reads back only the selected rows of the spill.  Otherwise the GEMM is
+ * followed by the finish of the unaligned verification path: decide, then
+ * in sampling mode the residual draw (two or three launches in all).
+ * Argument errors (M > 128, d not a multiple of 64, a misaligned operand,
+ * T < 0 or not finite, K > SV_MAX_K) return SV_ERR_INVALID, and a short or
+ * misaligned workspace SV_ERR_WORKSPACE, before any launch.
  */
 sv_status spec_lmhead_verify(const void *hidden, const void *w_vocab_t, int d, const float *q,
                              int B, int K, int V, float temperature, const int32_t *draft,

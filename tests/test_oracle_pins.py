@@ -428,13 +428,14 @@ def test_speedup_worked_examples(row):
 
 
 def test_expected_tokens_limits():
-    # E[N] in [1, gamma + 1] (AL ranges from 1 to 1 + D on page 1)
+    # E[N] in [1, gamma + 1]: AL lies between 1 and 1 + D ("Co-Designing AI Models Using Speculative
+    # Decoding for Faster LLM Inference", "What is speculative decoding?")
     for g in range(0, 9):
         assert speedup.expected_tokens(0.0, g) == 1.0
         assert speedup.expected_tokens(1.0, g) == g + 1
         assert abs(speedup.expected_tokens(0.999999, g) - (g + 1)) < 1e-4
-    # page 1's speedup reduces to AL when verification of B(1+D) costs the
-    # same as of B and drafting is free
+    # that section's speedup formula gives AL when verifying B(1+D) tokens costs
+    # the same as verifying B and drafting is free
     assert speedup.measured_speedup(2.0, 2.0, 0.0, 3.7) == pytest.approx(3.7)
 
 
