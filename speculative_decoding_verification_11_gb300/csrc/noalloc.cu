@@ -48,18 +48,25 @@ extern "C" sv_status spec_verify_sample_noalloc(const void *logits, sv_dtype dt,
                                                 int V, float temperature, const int32_t *draft,
                                                 const float *uniforms, int32_t *out_tokens,
                                                 int32_t *accept_len, float *diag, void *stream) {
-    if (B < 0 || K < 0 || K > SV_MAX_K || V <= 0) return SV_ERR_INVALID;
+    if (B < 0 || K < 0 || K > SV_MAX_K) return SV_ERR_INVALID;
+    // Every argument rule is checked before anything touches the shared
+    // scratch, so a refused call enqueues nothing.
+    const long long rows64 = static_cast<long long>(B) * (K + 1);
+    const sv_status arg = sv::check_verify_args(logits, dt, q, nullptr, B, K, rows64, V, temperature, true,
+                                                draft, uniforms, out_tokens, accept_len);
+    if (arg != SV_OK) return arg;
     if (B == 0) return spec_verify_sample(logits, dt, q, B, K, V, temperature, draft, uniforms, out_tokens,
                                           accept_len, diag, nullptr, 0, stream);
-    const int rows = B * (K + 1);
+    const int rows = static_cast<int>(rows64);
     if (spec_verify_workspace_size(B, rows, V) > SV_NOALLOC_SCRATCH_BYTES) return SV_ERR_WORKSPACE;
-    void *scratch = nullptr;
-    const sv_status st = scratch_address(&scratch);
-    if (st != SV_OK) return st;
     // The scratch keeps whatever the last call left in it; the per-request
     // counters must start this call at zero.
     size_t off = 0, bytes = 0;
     sv::counter_region(B, rows, V, &off, &bytes);
+    if (off > SV_NOALLOC_SCRATCH_BYTES || bytes > SV_NOALLOC_SCRATCH_BYTES - off) return SV_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    const sv_status st = scratch_address(&scratch);
+    if (st != SV_OK) return st;
     if (cudaMemsetAsync(static_cast<char *>(scratch) + off, 0, bytes, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return SV_ERR_CUDA;

@@ -12,6 +12,13 @@ void prof_begin(cudaStream_t s);   // profiling hook around the dominant kernel
 void prof_end(cudaStream_t s);
 void set_launches(int n);          // kernels launched by the last call (this thread)
 void counter_region(int B, int rows, int V, size_t *offset, size_t *bytes);  // per-request counters
+// Host-side argument rules of the verification calls (the workspace aside):
+// SV_ERR_INVALID if one is broken, else SV_OK.  `rows` is taken in 64 bits so
+// that a product B (K + 1) past INT_MAX is refused rather than wrapped.
+sv_status check_verify_args(const void *logits, sv_dtype dt, const float *q, const int32_t *row_offsets,
+                            int B, int K, long long rows, int V, float temperature, bool sample,
+                            const int32_t *draft, const float *uniforms, const int32_t *out_tokens,
+                            const int32_t *accept_len);
 size_t finish_workspace_size(int B, int rows, int V);
 // Decide (+ residual draw when `sample`) over fp32 logits and chunk partials
 // produced by a previous kernel on `s` (see verify.cu).

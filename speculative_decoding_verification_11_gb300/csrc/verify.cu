@@ -23,6 +23,7 @@
 // decoding?".  See include/specverify.h for the full contract.
 #include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -1807,22 +1808,37 @@ static std::atomic<size_t> g_small_limit{sk::kDefaultRowBytes};
 static std::atomic<int> g_cluster_on{1};
 
 // Common host path of the three logits-in entry points.
+// Host-side argument rules of every verification call (workspace aside):
+// SV_ERR_INVALID if one is broken, else SV_OK.  B = 0 passes (a no-op call).
+sv_status check_verify_args(const void *logits, sv_dtype dt, const float *q, const int32_t *row_offsets,
+                            int B, int K, long long rows, int V, float temperature, bool sample,
+                            const int32_t *draft, const float *uniforms, const int32_t *out_tokens,
+                            const int32_t *accept_len) {
+    if (B < 0 || V <= 0 || rows < 0 || (dt != SV_F32 && dt != SV_BF16)) return SV_ERR_INVALID;
+    if (!row_offsets && (K < 0 || K > SV_MAX_K)) return SV_ERR_INVALID;
+    if (B == 0) return SV_OK;
+    if (rows < B || rows > INT_MAX || rows * V >= (1ll << 62)) return SV_ERR_INVALID;
+    if (!logits || !out_tokens || !accept_len) return SV_ERR_INVALID;
+    if (rows > B && !draft) return SV_ERR_INVALID;
+    if (sample && (!(temperature > 0.f) || !std::isfinite(temperature) || !uniforms || (rows > B && !q)))
+        return SV_ERR_INVALID;
+    return SV_OK;
+}
+
 static sv_status verify_common(const void *logits, sv_dtype dt, const float *q,
-                               const int32_t *row_offsets, int B, int K, int rows, int V,
+                               const int32_t *row_offsets, int B, int K, long long rows64, int V,
                                float temperature, bool sample, const int32_t *draft,
                                const float *uniforms, int32_t *out_tokens, int32_t *accept_len,
                                float *diag, void *ws, size_t ws_bytes, void *stream) {
-    if (B < 0 || V <= 0 || rows < 0 || (dt != SV_F32 && dt != SV_BF16)) return SV_ERR_INVALID;
-    if (!row_offsets && (K < 0 || K > SV_MAX_K)) return SV_ERR_INVALID;
+    const sv_status arg = check_verify_args(logits, dt, q, row_offsets, B, K, rows64, V, temperature, sample,
+                                            draft, uniforms, out_tokens, accept_len);
+    if (arg != SV_OK) return arg;
     if (B == 0) {
         set_launches(0);
         return SV_OK;
     }
-    if (rows < B || static_cast<long long>(rows) * V >= (1ll << 62)) return SV_ERR_INVALID;
-    if (!logits || !out_tokens || !accept_len || !ws) return SV_ERR_INVALID;
-    if (rows > B && !draft) return SV_ERR_INVALID;
-    if (sample && (!(temperature > 0.f) || !std::isfinite(temperature) || !uniforms || (rows > B && !q)))
-        return SV_ERR_INVALID;
+    if (!ws) return SV_ERR_INVALID;
+    const int rows = static_cast<int>(rows64);
     const WsLayout L = ws_layout(B, rows, V);
     if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return SV_ERR_WORKSPACE;
 
@@ -1941,7 +1957,7 @@ extern "C" sv_status spec_verify_greedy(const void *logits, sv_dtype dt, int B, 
                                         int32_t *accept_len, void *ws, size_t ws_bytes,
                                         void *stream) {
     if (K < 0 || K > SV_MAX_K || B < 0) return SV_ERR_INVALID;
-    return verify_common(logits, dt, nullptr, nullptr, B, K, B * (K + 1), V, 0.f, false, draft,
+    return verify_common(logits, dt, nullptr, nullptr, B, K, static_cast<long long>(B) * (K + 1), V, 0.f, false, draft,
                          nullptr, out_tokens, accept_len, nullptr, ws, ws_bytes, stream);
 }
 
@@ -1951,7 +1967,7 @@ extern "C" sv_status spec_verify_sample(const void *logits, sv_dtype dt, const f
                                         int32_t *accept_len, float *diag, void *ws,
                                         size_t ws_bytes, void *stream) {
     if (K < 0 || K > SV_MAX_K || B < 0) return SV_ERR_INVALID;
-    return verify_common(logits, dt, q, nullptr, B, K, B * (K + 1), V, temperature, true, draft,
+    return verify_common(logits, dt, q, nullptr, B, K, static_cast<long long>(B) * (K + 1), V, temperature, true, draft,
                          uniforms, out_tokens, accept_len, diag, ws, ws_bytes, stream);
 }
 

@@ -122,3 +122,48 @@ def test_kv_argument_errors_return_before_launch(lib):
     assert lib.spec_kv_rollback(P, P, P, P, P, P, 4, 8, 16, 10, None, None) == binding.SV_ERR_INVALID
     assert lib.spec_kv_rollback(None, None, None, None, None, None, 0, 8, 16, 0, None, None) == binding.SV_OK
     del ok_args
+
+
+def test_noalloc_scratch_size_matches_the_header():
+    """The binding's copy of SV_NOALLOC_SCRATCH_BYTES is the header's value."""
+    src = open(HEADER).read()
+    m = re.search(r"#define\s+SV_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", src)
+    assert m, "SV_NOALLOC_SCRATCH_BYTES not found in the header"
+    assert binding.NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_noalloc_refuses_bad_arguments_before_touching_its_scratch(lib):
+    """Every argument rule of the allocation-free call is checked on the host
+    before its scratch is cleared: a refused call enqueues nothing (here no
+    CUDA call at all: this machine has no GPU, so reaching one would return
+    SV_ERR_CUDA instead of the refusal)."""
+    I = binding
+    call = lib.spec_verify_sample_noalloc
+    # B (K + 1) past INT_MAX: refused, not wrapped to a small or negative count
+    assert call(FAKE, 0, FAKE, 1 << 30, 1, 128, 1.0, FAKE, FAKE, FAKE, FAKE, None, None) == I.SV_ERR_INVALID
+    assert call(FAKE, 0, FAKE, (1 << 31) - 1, 255, 128, 1.0, FAKE, FAKE, FAKE, FAKE, None, None) == I.SV_ERR_INVALID
+    # null logits, outputs, draft, uniforms or q
+    assert call(None, 0, FAKE, 4, 2, 100, 1.0, FAKE, FAKE, FAKE, FAKE, None, None) == I.SV_ERR_INVALID
+    assert call(FAKE, 0, FAKE, 4, 2, 100, 1.0, FAKE, FAKE, None, FAKE, None, None) == I.SV_ERR_INVALID
+    assert call(FAKE, 0, FAKE, 4, 2, 100, 1.0, FAKE, FAKE, FAKE, None, None, None) == I.SV_ERR_INVALID
+    assert call(FAKE, 0, FAKE, 4, 2, 100, 1.0, None, FAKE, FAKE, FAKE, None, None) == I.SV_ERR_INVALID
+    assert call(FAKE, 0, FAKE, 4, 2, 100, 1.0, FAKE, None, FAKE, FAKE, None, None) == I.SV_ERR_INVALID
+    assert call(FAKE, 0, None, 4, 2, 100, 1.0, FAKE, FAKE, FAKE, FAKE, None, None) == I.SV_ERR_INVALID
+    # bad dtype, V, K, temperature
+    assert call(FAKE, 7, FAKE, 4, 2, 100, 1.0, FAKE, FAKE, FAKE, FAKE, None, None) == I.SV_ERR_INVALID
+    assert call(FAKE, 0, FAKE, 4, 2, 0, 1.0, FAKE, FAKE, FAKE, FAKE, None, None) == I.SV_ERR_INVALID
+    assert call(FAKE, 0, FAKE, 4, 256, 100, 1.0, FAKE, FAKE, FAKE, FAKE, None, None) == I.SV_ERR_INVALID
+    for T in (0.0, -1.0, float("inf"), float("nan")):
+        assert call(FAKE, 0, FAKE, 4, 2, 100, T, FAKE, FAKE, FAKE, FAKE, None, None) == I.SV_ERR_INVALID
+    # a valid call too large for the scratch: refused as a workspace error
+    assert call(FAKE, 0, FAKE, 20000, 4, 128256, 1.0, FAKE, FAKE, FAKE, FAKE, None, None) == I.SV_ERR_WORKSPACE
+
+
+def test_fixed_k_calls_refuse_row_counts_past_int_max(lib):
+    """B (K + 1) is formed in 64 bits: a product past INT_MAX is an argument
+    error, not a wrapped row count."""
+    I = binding
+    ws = ctypes.c_void_p(0x10000)
+    assert lib.spec_verify_greedy(FAKE, 0, 1 << 30, 1, 128, FAKE, FAKE, FAKE, ws, 1 << 20, None) == I.SV_ERR_INVALID
+    assert lib.spec_verify_sample(FAKE, 0, FAKE, 1 << 30, 3, 128, 1.0, FAKE, FAKE, FAKE, FAKE, None, ws, 1 << 20,
+                                  None) == I.SV_ERR_INVALID
