@@ -209,6 +209,25 @@ sv_status spec_draft_sample(const void *hidden, const void *w_vocab_t, int d, in
                             int32_t *x_out, float *u_out, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * The LM-head projection alone: logits = hidden . W_vocab in fp32, from the
+ * same tcgen05 GEMM (bf16 operands, fp32 accumulation in tensor memory over
+ * the hidden size in ascending order, 16 products per step) that feeds
+ * spec_lmhead_verify and spec_draft_sample ("Co-Designing AI Models Using
+ * Speculative Decoding for Faster LLM Inference", Guideline 1: the target's
+ * LM-head GEMM whose M grows from B to B (1 + D) under speculation).  For
+ * callers that want the target's logits themselves, e.g. to verify through
+ * spec_verify_sample, or to check the contraction on its own.
+ *   hidden     M x d bf16, row-major, 16-byte aligned; 1 <= M <= 128,
+ *              d a multiple of 64
+ *   w_vocab_t  V x d bf16 (row v = the weights of token v), 16-byte aligned
+ *   logits     M x V fp32, row-major, 16-byte aligned (written)
+ *   ws         spec_draft_workspace_size(M, d, V) bytes, 256-byte aligned
+ * One kernel on `stream`; argument errors return before any launch.
+ */
+sv_status spec_lmhead_logits(const void *hidden, const void *w_vocab_t, int d, int M, int V, float *logits,
+                             void *ws, size_t ws_bytes, void *stream);
+
+/*
  * Model-free n-gram (prompt lookup) drafter ("Co-Designing AI Models Using
  * Speculative Decoding for Faster LLM Inference", Table 1: suffix / n-gram
  * drafting matches strings over the token stream, no model, one lookup).
@@ -314,6 +333,23 @@ int spec_last_launch_count(void);
  * passes), or "none" before any such call.  A static string; for accounting.
  */
 const char *spec_last_kernel(void);
+
+/*
+ * Limit of the device-side waits, in SM clock cycles.  A kernel that waits on
+ * work other warps or CTAs produce (a ring stage, a row partial, a decision, a
+ * residual mass) gives up after `cycles` cycles from its start, sets
+ * SV_FLAG_TIMEOUT in the call's status word (spec_verify_last_device_status
+ * then returns SV_ERR_TIMEOUT), lets its own copies and MMAs in flight finish,
+ * releases what it holds and returns; its outputs are then undefined, and the
+ * workspace must be zero-filled again before its next use.  Waits on a CTA's
+ * own copies and MMAs keep a fixed limit of the same default, whatever this
+ * is set to.  cycles > 0 sets the limit, 0 restores the default (4e9 cycles,
+ * about 2 s at 2 GHz); returns the previous value, or -1 (and changes
+ * nothing) for cycles < 0.  Process-wide (an atomic), read by each call when
+ * it launches.  For callers that bound their latency, and for tests of the
+ * timeout path; the pages have no counterpart to it.
+ */
+long long spec_set_wait_budget(long long cycles);
 
 /*
  * Kernel choice for small vocabularies.  A call of spec_verify_greedy,

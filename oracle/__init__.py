@@ -13,6 +13,11 @@ Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``
                            plain argmax decoding, special cases.
   softmax_rows             pinned: closed forms.
   lmhead_logits            pinned: direct sum on small shapes.
+  gemm_bound.*             pinned: simulated fp32 accumulations (round to
+                           nearest and toward zero) stay inside the bound and
+                           reach a stated fraction of it; perturbed logits
+                           move p and the CDF inside the derived bands
+                           (tests/test_oracle_pins_gemm_bound.py).
   speedup.*                pinned: the worked numbers printed on the pages.
   kv_blocks.*              pinned: token-by-token simulation, conservation of
                            block ids, reserve + full rejection = identity,
@@ -65,7 +70,7 @@ def _load():
             P = ctypes.c_void_p
             lib.oracle_verify_batch.argtypes = [P, ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int64,
                                                 ctypes.c_double, ctypes.c_int, P, P, P, P, P, P, P,
-                                                ctypes.c_double]
+                                                ctypes.c_double, P, P]
             lib.oracle_verify_batch.restype = ctypes.c_int
             lib.oracle_softmax_row.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_double, P]
             lib.oracle_softmax_row.restype = None
@@ -106,12 +111,14 @@ def _ptr(a):
 
 
 def verify(logits, q, draft, uniforms, row_offsets, temperature: float, greedy: bool = False,
-           tie_band: float = 1e-6):
+           tie_band: float = 1e-6, p_rel_err=None, mass_err=None):
     """Run the oracle over a CSR batch.
 
     logits  (R, V) fp32 / bf16 / fp64;  q (R - B, V) fp32 (ignored if greedy);
     draft (R - B,) int32;  uniforms (R,) fp32 (ignored if greedy);
-    row_offsets (B + 1,) int32.  Returns a dict of numpy arrays:
+    row_offsets (B + 1,) int32.  p_rel_err (R - B,) and mass_err (R,) (fp64,
+    optional) widen the near-tie tests by known error bounds of the compared
+    side's p (see verify_oracle.c).  Returns a dict of numpy arrays:
       out_tokens (R,), accept_len (B,), p_draft (R - B,), residual_mass (B,),
       residual_prob (B,), near_tie_accept (B,), near_tie_sample (B,),
       zero_residual (B,), invalid (int).
@@ -141,10 +148,19 @@ def verify(logits, q, draft, uniforms, row_offsets, temperature: float, greedy: 
     pd = np.full(max(R - B, 1), np.nan, dtype=np.float64)
     req = np.full(2 * B, np.nan, dtype=np.float64)
     flags = np.zeros(3 * B, dtype=np.int32)
+    pre = me = None
+    if p_rel_err is not None:
+        pre = np.ascontiguousarray(np.asarray(p_rel_err, dtype=np.float64).reshape(-1))
+        if pre.shape[0] != R - B:
+            raise ValueError("p_rel_err needs one value per draft slot")
+    if mass_err is not None:
+        me = np.ascontiguousarray(np.asarray(mass_err, dtype=np.float64).reshape(-1))
+        if me.shape[0] != R:
+            raise ValueError("mass_err needs one value per logits row")
     rc = lib.oracle_verify_batch(_ptr(z), zcode, _ptr(qa), _ptr(ro), B, V,
                                  float(temperature if not greedy else 1.0), int(bool(greedy)),
                                  _ptr(x), _ptr(ua), _ptr(out), _ptr(al), _ptr(pd), _ptr(req),
-                                 _ptr(flags), float(tie_band))
+                                 _ptr(flags), float(tie_band), _ptr(pre), _ptr(me))
     if rc < 0:
         raise ValueError("malformed row_offsets")
     flags = flags.reshape(B, 3)
@@ -162,9 +178,9 @@ def verify(logits, q, draft, uniforms, row_offsets, temperature: float, greedy: 
 
 
 def verify_fixed(logits, q, draft, uniforms, B: int, K: int, temperature: float, greedy=False,
-                 tie_band: float = 1e-6):
+                 tie_band: float = 1e-6, p_rel_err=None, mass_err=None):
     ro = (np.arange(B + 1, dtype=np.int32) * (K + 1)).astype(np.int32)
-    return verify(logits, q, draft, uniforms, ro, temperature, greedy, tie_band)
+    return verify(logits, q, draft, uniforms, ro, temperature, greedy, tie_band, p_rel_err, mass_err)
 
 
 def softmax_rows(z, temperature: float) -> np.ndarray:
@@ -210,11 +226,21 @@ def lmhead_logits(hidden, w_vocab_t, v_chunk: int = 8192) -> np.ndarray:
 
 
 def lmhead_verify(hidden, w_vocab_t, q, draft, uniforms, B: int, K: int, temperature: float,
-                  tie_band: float = 1e-6):
+                  tie_band: float = 1e-6, bands=None):
     """Fused front end + verification: fp64 GEMM, then the same steps as verify().
-    Returns the verify() dict plus the fp64 logits under "logits"."""
-    z = lmhead_logits(hidden, w_vocab_t)
+    Returns the verify() dict plus the fp64 logits under "logits".
+
+    bands: None, or a gemm_bound.Bands of this batch (the fp64 logits, their
+    accumulation bound and the induced p and mass error bounds, from
+    gemm_bound.bands()); its logits are used and its bounds widen the near-tie
+    tests.  In greedy mode the bands are not used here (see
+    gemm_bound.greedy_flip_possible)."""
+    z = lmhead_logits(hidden, w_vocab_t) if bands is None else bands.logits
     greedy = temperature == 0
-    res = verify_fixed(z, q, draft, uniforms, B, K, temperature if not greedy else 1.0, greedy, tie_band)
+    pre = me = None
+    if bands is not None and not greedy:
+        pre, me = bands.p_rel_err_at(draft, B, K), bands.mass_err
+    res = verify_fixed(z, q, draft, uniforms, B, K, temperature if not greedy else 1.0, greedy, tie_band,
+                       pre, me)
     res["logits"] = z
     return res

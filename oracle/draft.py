@@ -64,11 +64,17 @@ def draw_inverse_cdf(r, u: float, band: float = 1e-6):
     return int(v), bool(nt.value)
 
 
-def draft_sample(hidden, w_vocab_t, temperature: float, seed: int, offset: int = 0, tie_band: float = 1e-4):
+def draft_sample(hidden, w_vocab_t, temperature: float, seed: int, offset: int = 0, tie_band: float = 1e-6,
+                 bands=None):
     """hidden (M, d) bf16, w_vocab_t (V, d) bf16.  Returns a dict: logits (fp64),
     q (M, V) fp64 or None (greedy), u (M,) (fp64, exactly representable in
-    fp32), x (M,) int32, near_tie (M,) bool."""
-    z = lmhead_logits(hidden, w_vocab_t)
+    fp32), x (M,) int32, near_tie (M,) bool.
+
+    bands: None, or the gemm_bound.Bands of these operands at this
+    temperature: its logits are used, and row r's draw is a near tie when a
+    CDF boundary lies within tie_band + 2 E_r / (1 - E_r) of u (E_r its bound
+    on the error of the row's probability masses, whose total is 1)."""
+    z = lmhead_logits(hidden, w_vocab_t) if bands is None else bands.logits
     M = z.shape[0]
     if temperature == 0:
         x = argmax_rows(z).astype(np.int32)
@@ -78,5 +84,9 @@ def draft_sample(hidden, w_vocab_t, temperature: float, seed: int, offset: int =
     x = np.zeros(M, dtype=np.int32)
     nt = np.zeros(M, dtype=bool)
     for r in range(M):
-        x[r], nt[r] = draw_inverse_cdf(q[r], u[r], tie_band)
+        band = tie_band
+        if bands is not None:
+            E = float(bands.mass_err[r])
+            band = tie_band + 2.0 * E / (1.0 - E) if E < 1.0 else np.inf
+        x[r], nt[r] = draw_inverse_cdf(q[r], u[r], band)
     return {"logits": z, "q": q, "u": u, "x": x, "near_tie": nt}

@@ -33,10 +33,17 @@
  *   - a drafted id outside [0, V) invalidates its request: AL = 0, all -1.
  *
  * Near ties (decisions the parity rule lets differ) are flagged here in fp64:
- *   accept test: q > 0 and |u - p/q| < band;
- *   final sample: a CDF boundary C(v)/R within band of u;
- * band = 1e-6 unless the caller passes another (the fused LM-head path, whose
- * logits carry the GEMM's fp32 accumulation error, uses a wider one).
+ *   accept test: q > 0 and |u - p/q| < band + e_p p/q;
+ *   final sample: a CDF boundary C(v)/R within band + 2 E / (R - E) of u
+ *                 (every boundary is a near tie when E >= R);
+ * band = 1e-6 unless the caller passes another.  e_p (per draft slot: a bound
+ * on the relative error of p at the drafted token) and E (per logits row: a
+ * bound on the absolute error of the row's probability masses, which bounds
+ * the error of C and R alike) are zero unless the caller passes them: the
+ * fused LM-head path does, from the error bound of its GEMM's fp32
+ * accumulation.  Since the compared quantity p/q then carries a relative error
+ * of at most e_p, and C and R an absolute one of at most E, the GPU's decision
+ * can differ from the fp64 one only inside these bands.
  */
 #include <math.h>
 #include <stdint.h>
@@ -116,12 +123,17 @@ int64_t oracle_argmax_row(const void *z, int dtype, int64_t V)
  *   flags : 3 values: near-tie accept count, near-tie final-sample flag,
  *           zero-residual flag
  *   work  : 2 V doubles of scratch
+ *   p_rel_err  : K values (may be NULL = 0): bound on the relative error of
+ *                the compared p_j(x_j)
+ *   mass_err   : K+1 values (may be NULL = 0): bound on the absolute error of
+ *                the probability masses of row j
  * Returns 0, or 1 when a drafted id is out of range.
  */
 int oracle_verify_request(const void *z, int zdtype, const float *q, const int32_t *x,
                           const float *u, int K, int64_t V, double T, int greedy,
                           int32_t *out, int32_t *al, double *p_draft, double *req,
-                          int32_t *flags, double *work, double tie_band)
+                          int32_t *flags, double *work, double tie_band,
+                          const double *p_rel_err, const double *mass_err)
 {
     for (int j = 0; j <= K; ++j)
         out[j] = -1;
@@ -160,7 +172,8 @@ int oracle_verify_request(const void *z, int zdtype, const float *q, const int32
         double qj = (double)q[(int64_t)j * V + x[j]];
         double uj = (double)u[j];
         p_draft[j] = pj;
-        if (qj > 0.0 && fabs(uj - pj / qj) < tie_band)
+        double ep = p_rel_err ? p_rel_err[j] : 0.0;
+        if (qj > 0.0 && fabs(uj - pj / qj) < tie_band + ep * (pj / qj))
             flags[0] += 1;
         if (!(uj * qj <= pj)) {
             kstar = j;
@@ -194,6 +207,8 @@ int oracle_verify_request(const void *z, int zdtype, const float *q, const int32
         flags[2] = 1;
     }
 
+    double E = mass_err ? mass_err[kstar] : 0.0;
+    double band = E < R ? tie_band + 2.0 * E / (R - E) : INFINITY;
     double ufin = (double)u[K];
     double t = ufin * R;
     double C = 0.0, Cprev = 0.0;
@@ -214,7 +229,7 @@ int oracle_verify_request(const void *z, int zdtype, const float *q, const int32
             }
         }
         flags[1] = 1;
-    } else if (ufin - Cprev / R < tie_band || C / R - ufin < tie_band) {
+    } else if (ufin - Cprev / R < band || C / R - ufin < band) {
         flags[1] = 1;
     }
     out[kstar] = (int32_t)vstar;
@@ -230,13 +245,16 @@ int oracle_verify_request(const void *z, int zdtype, const float *q, const int32
  * slots row_offsets[b] .. row_offsets[b+1]-1 and draft ids / q rows
  * row_offsets[b]-b .. row_offsets[b+1]-b-2.
  *   p_draft : (rows - B) values, req : 2 B values, flags : 3 B values.
+ *   p_rel_err : (rows - B) values, mass_err : rows values (either may be NULL),
+ *               the error bounds of oracle_verify_request laid out like the
+ *               draft slots and the logits rows.
  * Returns -1 for malformed offsets, else the number of invalid requests.
  */
 int oracle_verify_batch(const void *logits, int zdtype, const float *q,
                         const int32_t *row_offsets, int B, int64_t V, double T, int greedy,
                         const int32_t *draft, const float *uniforms, int32_t *out_tokens,
                         int32_t *accept_len, double *p_draft, double *req, int32_t *flags,
-                        double tie_band)
+                        double tie_band, const double *p_rel_err, const double *mass_err)
 {
     if (!(tie_band > 0.0))
         tie_band = NEAR_TIE_DEFAULT;
@@ -259,7 +277,8 @@ int oracle_verify_batch(const void *logits, int zdtype, const float *q,
         float dummy_u[1] = {0.5f};
         bad += oracle_verify_request(z, zdtype, qb, draft + d0, ub ? ub : dummy_u, K, V, T,
                                      greedy, out_tokens + r0, accept_len + b, p_draft + d0,
-                                     req + 2 * b, flags + 3 * b, work, tie_band);
+                                     req + 2 * b, flags + 3 * b, work, tie_band,
+                                     p_rel_err ? p_rel_err + d0 : NULL, mass_err ? mass_err + r0 : NULL);
     }
     free(work);
     return bad;

@@ -29,6 +29,7 @@ EXPORTS = (
     "spec_verify_sample_noalloc", "spec_set_small_kernel_limit", "spec_set_cluster_kernel",
     "spec_kv_reserve", "spec_kv_rollback",
     "spec_draft_workspace_size", "spec_draft_sample", "spec_ngram_draft", "spec_dynk_update",
+    "spec_lmhead_logits", "spec_set_wait_budget",
 )
 
 _lock = threading.Lock()
@@ -77,6 +78,8 @@ def load() -> ctypes.CDLL:
             "spec_draft_sample": (I, [P, P, I, I, I, F, ctypes.c_uint64, ctypes.c_uint64, P, P, P, P, Z, P]),
             "spec_ngram_draft": (I, [P, P, I, I, I, I, P, P, P]),
             "spec_dynk_update": (I, [P, P, P, P, I, I, I, F, I, I, P, F, P, P, P]),
+            "spec_lmhead_logits": (I, [P, P, I, I, I, P, P, Z, P]),
+            "spec_set_wait_budget": (ctypes.c_longlong, [ctypes.c_longlong]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -262,6 +265,15 @@ def bind_spec_profile_set_events(begin=None, end=None):
     return call
 
 
+def spec_set_wait_budget(cycles: int) -> int:
+    """Device-side wait limit in SM cycles (0 restores the default); returns the
+    previous value."""
+    prev = int(load().spec_set_wait_budget(int(cycles)))
+    if prev < 0:
+        raise ValueError("cycles must be >= 0")
+    return prev
+
+
 def spec_set_small_kernel_limit(nbytes: int) -> int:
     """Largest per-request logits footprint (bytes) that runs on the
     request-per-CTA kernel; 0 sends every call to the streaming kernel.
@@ -327,6 +339,19 @@ def spec_draft_sample(hidden, w_vocab_t, temperature, seed, offset, q_out, x_out
                                   int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(q_out), _ptr(x_out),
                                   _ptr(u_out), _ptr(ws), ws.numel(), _stream(stream))
     _raise(st, "spec_draft_sample")
+
+
+def spec_lmhead_logits(hidden, w_vocab_t, logits, ws, stream=None):
+    """logits (M x V fp32) = hidden (M x d bf16) . w_vocab_t (V x d bf16)^T on
+    the LM-head GEMM; ws of spec_draft_workspace_size(M, d, V) bytes."""
+    _check(hidden, torch.bfloat16, None, "hidden")
+    _check(w_vocab_t, torch.bfloat16, None, "w_vocab_t")
+    M, d = hidden.shape
+    V = w_vocab_t.shape[0]
+    _check(logits, torch.float32, M * V, "logits")
+    st = load().spec_lmhead_logits(_ptr(hidden), _ptr(w_vocab_t), d, M, V, _ptr(logits), _ptr(ws), ws.numel(),
+                                   _stream(stream))
+    _raise(st, "spec_lmhead_logits")
 
 
 def spec_ngram_draft(tokens, ctx_offsets, K, n_min, n_max, draft_out, k_out, stream=None):

@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 2) cluster_kernel(Args a) {
         s_q[tid] = qj;
         s_u[tid] = uj;
     }
-    if (nt > 0 && !mbar_wait_bounded(&s_bar, 0, kWaitBudget) && tid == 0) atomicOr(a.status, SV_FLAG_TIMEOUT);
+    if (nt > 0 && !mbar_wait_bounded(&s_bar, 0, kDrainBudget) && tid == 0) atomicOr(a.status, SV_FLAG_TIMEOUT);
 
     // row partials over the slice: row j takes warps [j wpr, (j + 1) wpr), each a part in token order
     const int wpr = nr <= kWarps ? kWarps / nr : 1;

@@ -31,6 +31,7 @@
 #include <mutex>
 
 #include "../../include/specverify.h"
+#include "sv_args.cuh"
 #include "sv_device.cuh"
 #include "sv_draw.cuh"
 #include "sv_host.h"
@@ -45,7 +46,6 @@ constexpr int UK = 16;                  // K of one tcgen05.mma kind::f16
 constexpr int kABytes = BM * BK * 2;    // 16 KB
 constexpr int kEpiWarps = 4;
 constexpr int kThreadsLm = (2 + kEpiWarps) * 32;
-constexpr long long kLmWaitBudget = 4000000000ll;
 constexpr int kLmSmemBudget = 204800;   // shared bytes for the operand ring
 
 // Vocabulary tile width BN (a multiple of 32, <= 256) and the ring depth that
@@ -83,6 +83,7 @@ struct LmArgs {
     int spill_tma;    // 1: the spill is written by bulk tensor stores through the third tensor map
     float2 *partials; // M x gridDim.x: one merged partial per row and CTA
     uint32_t *status;
+    long long wait_budget;  // SM cycles a wait on another warp's work may take (own copies and MMAs: kDrainBudget)
 };
 
 // ---------------------------------------------------------------------------
@@ -246,7 +247,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                 for (int kb = 0; kb < nk; ++kb, ++kg) {
                     const int s = kg % kStagesLm;
                     if (kg >= kStagesLm &&
-                        !mbar_wait_bounded(&sm.empty[s], ((kg / kStagesLm) - 1) & 1, kLmWaitBudget)) {
+                        !mbar_wait_bounded(&sm.empty[s], ((kg / kStagesLm) - 1) & 1, a.wait_budget)) {
                         timeout();
                         break;
                     }
@@ -257,14 +258,14 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
             }
             // let every copy issued into the ring land before the CTA can leave
             for (int kk = max(0, kg - kStagesLm); kk < kg; ++kk)
-                mbar_wait_bounded(&sm.full[kk % kStagesLm], (kk / kStagesLm) & 1, kLmWaitBudget);
+                mbar_wait_bounded(&sm.full[kk % kStagesLm], (kk / kStagesLm) & 1, kDrainBudget);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             int kg = 0, ti = 0;
             for (int t = blockIdx.x; t < a.n_tiles && !*abort_flag; t += gridDim.x, ++ti) {
                 const int buf = ti & 1;
-                if (ti >= 2 && !mbar_wait_bounded(&sm.acc_empty[buf], ((ti / 2) - 1) & 1, kLmWaitBudget)) {
+                if (ti >= 2 && !mbar_wait_bounded(&sm.acc_empty[buf], ((ti / 2) - 1) & 1, a.wait_budget)) {
                     timeout();
                     break;
                 }
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                 bool ok = true;
                 for (int kb = 0; kb < nk; ++kb, ++kg) {
                     const int s = kg % kStagesLm;
-                    if (!mbar_wait_bounded(&sm.full[s], (kg / kStagesLm) & 1, kLmWaitBudget)) {
+                    if (!mbar_wait_bounded(&sm.full[s], (kg / kStagesLm) & 1, a.wait_budget)) {
                         timeout();
                         ok = false;
                         break;
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
             }
             // all issued MMAs complete before TMEM is released
             tc_commit(&sm.mma_done);
-            mbar_wait_bounded(&sm.mma_done, 0, kLmWaitBudget);
+            mbar_wait_bounded(&sm.mma_done, 0, kDrainBudget);  // own MMAs, before TMEM is released
         }
     } else {
         // epilogue: warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
         int ti = 0;
         for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++ti) {
             const int buf = ti & 1;
-            if (!mbar_wait_bounded(&sm.acc_full[buf], (ti / 2) & 1, kLmWaitBudget)) timeout();
+            if (!mbar_wait_bounded(&sm.acc_full[buf], (ti / 2) & 1, a.wait_budget)) timeout();
             if (*abort_flag) break;
             tc_fence_after();
             const int n0 = t * BN;
@@ -1034,6 +1035,7 @@ extern "C" sv_status spec_lmhead_verify(const void *hidden, const void *w_vocab_
     a.spill = sample ? reinterpret_cast<float *>(w + L.spill) : nullptr;
     a.partials = reinterpret_cast<float2 *>(w + L.partials);
     a.status = reinterpret_cast<uint32_t *>(w + L.finish);  // the status word is the workspace's first word
+    a.wait_budget = wait_budget();
     // the cluster finish reads back only the selected rows and discards the rest from L2
     const bool cluster_finish = V % 4 == 0 && lm::fin_segs_per_cta(V) <= lm::kFinMaxSegs &&
                                 (!sample || K == 0 || (reinterpret_cast<uintptr_t>(q) & 15u) == 0);
@@ -1129,6 +1131,7 @@ extern "C" sv_status spec_draft_sample(const void *hidden, const void *w_vocab_t
     a.spill_tma = (sample && lm::encode_f32_rows(&tc, a.spill, M, V)) ? 1 : 0;  // V % 4 == 0 here
     a.partials = reinterpret_cast<float2 *>(w + 256);
     a.status = reinterpret_cast<uint32_t *>(w);
+    a.wait_budget = wait_budget();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     prof_begin(s);
     if (sample) lm::launch_gemm_bn<true>(bn, ta, tb, tc, a, grid, s);
@@ -1152,4 +1155,46 @@ extern "C" sv_status spec_draft_sample(const void *hidden, const void *w_vocab_t
                                                       offset, x_out, u_out);
     set_launches(2);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+extern "C" sv_status spec_lmhead_logits(const void *hidden, const void *w_vocab_t, int d, int M, int V,
+                                        float *logits, void *ws, size_t ws_bytes, void *stream) {
+    if (M < 0 || M > lm::BM || V <= 0 || d < lm::BK || d % lm::BK != 0) return SV_ERR_INVALID;
+    if (M == 0) {
+        set_launches(0);
+        return SV_OK;
+    }
+    if (!hidden || !w_vocab_t || !logits || !ws) return SV_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(hidden) & 15u) || (reinterpret_cast<uintptr_t>(w_vocab_t) & 15u) ||
+        (reinterpret_cast<uintptr_t>(logits) & 15u))
+        return SV_ERR_INVALID;
+    if (ws_bytes < spec_draft_workspace_size(M, d, V) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return SV_ERR_WORKSPACE;
+    const int bn = lm::choose_bn(V, sm_count());
+    const int n_tiles = (V + bn - 1) / bn;
+    int grid = n_tiles < sm_count() ? n_tiles : sm_count();
+    if (grid > lm::kMaxLmGrid) grid = lm::kMaxLmGrid;
+    CUtensorMap ta, tb;
+    if (!lm::encode_bf16_kmajor(&ta, hidden, M, d, lm::BM) || !lm::encode_bf16_kmajor(&tb, w_vocab_t, V, d, bn))
+        return SV_ERR_CUDA;
+    char *w = static_cast<char *>(ws);
+    lm::LmArgs a;
+    a.M = M;
+    a.d = d;
+    a.V = V;
+    a.n_tiles = n_tiles;
+    a.c = 1.4426950408889634f;  // the row partials it also writes are those of T = 1 (unused here)
+    a.spill = logits;
+    a.spill_keep = 0;
+    CUtensorMap tc = tb;
+    a.spill_tma = (V % 4 == 0 && lm::encode_f32_rows(&tc, logits, M, V)) ? 1 : 0;
+    a.partials = reinterpret_cast<float2 *>(w + 256);
+    a.status = reinterpret_cast<uint32_t *>(w);
+    a.wait_budget = wait_budget();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    prof_begin(s);
+    lm::launch_gemm_bn<true>(bn, ta, tb, tc, a, grid, s);
+    prof_end(s);
+    set_launches(1);
+    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

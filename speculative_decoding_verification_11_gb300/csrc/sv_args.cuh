@@ -53,9 +53,19 @@ struct Args {
     int tail_b0;         // fused kernel: requests from here on take one-stage residual claims
     int early_res;       // fused kernel: residual claims may start during the stats stream
     float *cv_segs;      // cluster kernel: per request, one residual sum per 256-token segment
+    long long wait_budget;  // SM cycles a wait on other warps' or CTAs' work may take
 };
 
-constexpr long long kWaitBudget = 4000000000ll;  // SM cycles (~2 s) before a wait gives up
+// Two kinds of bounded waits.  A wait on work that other warps or CTAs
+// produce (a ring stage, a partial, a decision, a segment mass) gives up after
+// Args::wait_budget SM cycles (spec_set_wait_budget; default kDefaultWaitBudget,
+// ~2 s at 2 GHz), then flags SV_FLAG_TIMEOUT and leaves.  A wait on the CTA's
+// own copies or MMAs, before it leaves or releases what they write, always
+// allows kDrainBudget: those complete by themselves in microseconds, and a CTA
+// may not leave while a copy into its shared memory is still landing, however
+// short the other budget is set.
+constexpr long long kDefaultWaitBudget = 4000000000ll;
+constexpr long long kDrainBudget = 4000000000ll;
 
 __device__ __forceinline__ void request_rows(const Args &a, int b, int &r0, int &nr) {
     if (a.row_offsets) {

@@ -11,6 +11,7 @@ int sm_count();                    // SMs of the current device
 void prof_begin(cudaStream_t s);   // profiling hook around the dominant kernel
 void prof_end(cudaStream_t s);
 void set_launches(int n);          // kernels launched by the last call (this thread)
+long long wait_budget();           // spec_set_wait_budget's current value (SM cycles)
 void counter_region(int B, int rows, int V, size_t *offset, size_t *bytes);  // per-request counters
 // Host-side argument rules of the verification calls (the workspace aside):
 // SV_ERR_INVALID if one is broken, else SV_OK.  `rows` is taken in 64 bits so

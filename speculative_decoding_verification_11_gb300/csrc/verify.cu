@@ -877,7 +877,7 @@ __device__ __forceinline__ bool give_up(const Args &a, volatile int *abort_flag,
     int stop = 0;
     if (lane == 0) {
         stop = *abort_flag;
-        if (!stop && clock64() - t_start > kWaitBudget) {
+        if (!stop && clock64() - t_start > a.wait_budget) {
             *abort_flag = 1;
             atomicOr(a.status, SV_FLAG_TIMEOUT);
             stop = 1;
@@ -1260,7 +1260,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
             // next ring stage: wait until the consumers released it
             auto claim = [&](int &s) -> bool {
                 s = k % kStages;
-                if (k >= kStages && !mbar_wait_bounded(&sm.empty[s], ((k / kStages) - 1) & 1, kWaitBudget)) {
+                if (k >= kStages && !mbar_wait_bounded(&sm.empty[s], ((k / kStages) - 1) & 1, a.wait_budget)) {
                     timeout();
                     return false;
                 }
@@ -1391,7 +1391,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                             ok = false;
                             break;
                         }
-                        if (clock64() - t_start > kWaitBudget) {
+                        if (clock64() - t_start > a.wait_budget) {
                             timeout();
                             ok = false;
                             break;
@@ -1427,7 +1427,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
                 mbar_arrive(&sm.full[s]);
             } else {
                 for (int kk = max(0, k - kStages); kk < k; ++kk)
-                    mbar_wait_bounded(&sm.full[kk % kStages], (kk / kStages) & 1, kWaitBudget);
+                    mbar_wait_bounded(&sm.full[kk % kStages], (kk / kStages) & 1, kDrainBudget);  // own copies
             }
         }
         // This CTA streams nothing more.  The last producer out resets the scheduling counters
@@ -1469,7 +1469,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(Args a) {
         partial_identity<kSample>(ra, rb);
         for (int k = 0;; ++k) {
             const int s = k % kStages;
-            if (!mbar_wait_bounded(&sm.full[s], (k / kStages) & 1, kWaitBudget)) timeout();
+            if (!mbar_wait_bounded(&sm.full[s], (k / kStages) & 1, a.wait_budget)) timeout();
             if (*abort_flag) break;
             const Tag tg = sm.tag[s];
             if (tg.kind == kEnd) break;
@@ -1806,8 +1806,10 @@ static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 static std::atomic<size_t> g_small_limit{sk::kDefaultRowBytes};
 // Whether small batches of medium requests may run on cv::cluster_kernel.
 static std::atomic<int> g_cluster_on{1};
+// Limit of the waits on other warps' or CTAs' work (spec_set_wait_budget).
+static std::atomic<long long> g_wait_budget{kDefaultWaitBudget};
+long long wait_budget() { return g_wait_budget.load(std::memory_order_relaxed); }
 
-// Common host path of the three logits-in entry points.
 // Host-side argument rules of every verification call (workspace aside):
 // SV_ERR_INVALID if one is broken, else SV_OK.  B = 0 passes (a no-op call).
 sv_status check_verify_args(const void *logits, sv_dtype dt, const float *q, const int32_t *row_offsets,
@@ -1825,6 +1827,7 @@ sv_status check_verify_args(const void *logits, sv_dtype dt, const float *q, con
     return SV_OK;
 }
 
+// Common host path of the three logits-in entry points.
 static sv_status verify_common(const void *logits, sv_dtype dt, const float *q,
                                const int32_t *row_offsets, int B, int K, long long rows64, int V,
                                float temperature, bool sample, const int32_t *draft,
@@ -1860,6 +1863,7 @@ static sv_status verify_common(const void *logits, sv_dtype dt, const float *q,
     a.n_draft = rows - B;
     a.c = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(temperature)) : 1.f;
     a.status = reinterpret_cast<uint32_t *>(w + L.status);
+    a.wait_budget = wait_budget();
     a.csr_ok = row_offsets ? reinterpret_cast<const int *>(w + L.csr_ok) : nullptr;
     set_ws_records(a, w, L);
     a.dec = reinterpret_cast<Decision *>(w + L.dec);
@@ -1922,6 +1926,7 @@ sv_status finish_from_partials(const float *logits, const float2 *partials, int 
     a.n_draft = rows - B;
     a.c = sample ? static_cast<float>(1.4426950408889634 / static_cast<double>(temperature)) : 1.f;
     a.status = reinterpret_cast<uint32_t *>(w + L.status);
+    a.wait_budget = wait_budget();
     a.csr_ok = nullptr;
     set_ws_records(a, w, L);
     a.dec = reinterpret_cast<Decision *>(w + L.dec);
@@ -2023,6 +2028,11 @@ extern "C" const char *spec_last_kernel(void) { return g_last_kernel; }
 
 extern "C" int spec_set_cluster_kernel(int enable) {
     return g_cluster_on.exchange(enable != 0 ? 1 : 0, std::memory_order_relaxed);
+}
+
+extern "C" long long spec_set_wait_budget(long long cycles) {
+    if (cycles < 0) return -1;
+    return g_wait_budget.exchange(cycles == 0 ? kDefaultWaitBudget : cycles, std::memory_order_relaxed);
 }
 
 extern "C" size_t spec_set_small_kernel_limit(size_t bytes) {

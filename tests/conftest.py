@@ -19,3 +19,13 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.fail("GPU test selected but no CUDA device is visible")
     return torch.device("cuda:0")
+
+
+@pytest.fixture(scope="session")
+def lmhead_full():
+    """The fused LM-head workload (B=16, K=7, d=8192, V=128256, T=1) with its
+    fp64 logits and their accumulation bound (oracle.gemm_bound), built once."""
+    from oracle import gemm_bound
+    from speculative_decoding_verification_11_gb300 import workloads
+    b = workloads.lmhead()
+    return b, gemm_bound.bands(b.hidden, b.w_vocab_t, b.temperature)

@@ -167,3 +167,17 @@ def test_fixed_k_calls_refuse_row_counts_past_int_max(lib):
     assert lib.spec_verify_greedy(FAKE, 0, 1 << 30, 1, 128, FAKE, FAKE, FAKE, ws, 1 << 20, None) == I.SV_ERR_INVALID
     assert lib.spec_verify_sample(FAKE, 0, FAKE, 1 << 30, 3, 128, 1.0, FAKE, FAKE, FAKE, FAKE, None, ws, 1 << 20,
                                   None) == I.SV_ERR_INVALID
+
+
+def test_wait_budget_knob(lib):
+    """spec_set_wait_budget: returns the previous value, 0 restores the default,
+    a negative value is refused and changes nothing (host only, no launch)."""
+    default = 4000000000
+    prev = binding.spec_set_wait_budget(1234)
+    try:
+        assert prev == default
+        assert lib.spec_set_wait_budget(-5) == -1
+        assert binding.spec_set_wait_budget(0) == 1234
+        assert binding.spec_set_wait_budget(0) == default
+    finally:
+        binding.spec_set_wait_budget(0)
