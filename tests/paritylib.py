@@ -7,7 +7,10 @@
            counted and reported, never silently passed.
            p_j(x_j) within 1e-5 relative; the residual mass R and the drawn
            token's probability r(v*)/R within 1e-5 relative plus an absolute
-           allowance for fp32 cancellation in p - q (see DESIGN notes).
+           allowance of 4e-7 / R: r = p - q is a difference of two
+           probabilities, so the fp32 rounding of p (about 2^-22 relative)
+           becomes an absolute error in r that a relative bound cannot cover
+           when p and q are close.
 """
 from __future__ import annotations
 
