@@ -6,14 +6,19 @@
 // Decoding" (glossary), section "Variants: Draft Models, EAGLE, Medusa, and
 // Model-Free Methods" (prompt lookup matches strings already in the context).
 //
-// One CTA per request.  The context's last n_max tokens sit in shared memory,
-// and the context passes through shared memory in tiles of 8192 tokens (with
-// the 32 tokens before each tile kept as a halo); every thread takes
-// candidate end positions e <= L - 2 and measures m(e),
-// the length of the common suffix of ctx[..e] and ctx[..L-1] (at most
-// min(n_max, e + 1)).  The winner maximises (m, e) with m >= n_min: the
-// longest suffix first, then its latest occurrence -- the order in which the
-// method tries n = n_max .. n_min and scans back from the end.
+// One cluster of kSplit CTAs per request: CTA s of the cluster takes the
+// s-th quarter of the candidate end positions e <= L - 2 and measures, for
+// each, m(e), the length of the common suffix of ctx[..e] and ctx[..L-1] (at
+// most min(n_max, e + 1)); its range of the context (with the kMaxN tokens
+// before it) passes through shared memory in tiles of kTile tokens, copied
+// asynchronously.  The winner maximises (m, e) with m >= n_min: the longest
+// suffix first, then its latest occurrence -- the order in which the method
+// tries n = n_max .. n_min and scans back from the end.  Each CTA's best
+// (m, e) goes to the first CTA of the cluster through distributed shared
+// memory; that CTA writes the proposal.  Splitting a context over four CTAs
+// divides its copy latency and its compares by four; the compares read four
+// candidate ends at a time and test them against the context's last token
+// first, so that only the few that match it are extended.
 #include <cstdint>
 
 #include "../../include/specverify.h"
@@ -23,57 +28,67 @@
 namespace sv {
 namespace ng {
 
-constexpr int kThreads = 512;
+constexpr int kSplit = 4;       // CTAs per request (one cluster)
+constexpr int kThreads = 256;
 constexpr int kMaxN = 32;
-constexpr int kTile = 8192;            // context tokens staged in shared memory at a time
-constexpr int kPerThread = kTile / kThreads;
+constexpr int kTile = 4096;     // candidate ends (and context tokens) staged in shared memory at a time
+
+__device__ __forceinline__ void cp_async_4(int32_t *dst, const int32_t *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
 
 __global__ void __launch_bounds__(kThreads) ngram_kernel(const int32_t *tokens, const int32_t *ctx_offsets, int K,
                                                          int n_min, int n_max, int32_t *draft_out, int32_t *k_out) {
+    cluster_arrive_relaxed();  // matched by the wait before the first remote store
     pdl_wait_prior_grid();
     pdl_launch_dependents();
-    // buf[kMaxN + i] = ctx[t0 + i]; buf[0 .. kMaxN) holds the kMaxN tokens before the tile (the halo)
-    __shared__ int32_t buf[kMaxN + kTile];
+    // buf[kMaxN + i] = ctx[t0 + i]; buf[0 .. kMaxN) = the kMaxN tokens before the tile (zero before ctx[0])
+    __shared__ __align__(16) int32_t buf[kMaxN + kTile + 4];
     __shared__ int32_t suf[kMaxN];
     __shared__ unsigned long long s_best[kThreads / 32];
-    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __shared__ unsigned long long s_keys[kSplit];  // the first CTA: every CTA's best key
+    const int b = blockIdx.x, part = static_cast<int>(cluster_ctarank());
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long s0 = ctx_offsets[b];
     long long L = static_cast<long long>(ctx_offsets[b + 1]) - s0;
     if (L < 0) L = 0;  // decreasing offsets: an empty context, nothing proposed
     const int32_t *ctx = tokens + s0;
     if (tid < n_max && tid < L) suf[tid] = ctx[L - 1 - tid];
+    const long long n_cand = L >= 2 ? L - 1 : 0;  // candidate ends 0 .. L - 2
+    const long long chunk = (n_cand + kSplit - 1) / kSplit;
+    const long long c0 = part * chunk, c1 = (c0 + chunk < n_cand) ? c0 + chunk : n_cand;
     // key = m << 32 | e, 0 = no candidate (m >= n_min >= 1 makes every real key nonzero)
     unsigned long long best = 0ull;
-    int32_t v[kPerThread];  // the next tile, loaded while the current one is compared
-#pragma unroll
-    for (int j = 0; j < kPerThread; ++j) {
-        const long long i = j * kThreads + tid;
-        v[j] = i < L ? ctx[i] : 0;
-    }
-    for (long long t0 = 0; t0 <= L - 2; t0 += kTile) {
-        const long long n_here = (L - 1 - t0) < kTile ? (L - 1 - t0) : kTile;  // candidate ends t0 .. t0 + n_here - 1
-        __syncthreads();  // the previous tile's compares are done
-        if (tid < kMaxN) {
-            const long long i = t0 - kMaxN + tid;
-            buf[tid] = (t0 > 0 && i >= 0) ? buf[kTile + tid] : 0;  // last kMaxN tokens of the previous tile
+    for (long long t0 = c0; t0 < c1; t0 += kTile) {
+        const int n_here = static_cast<int>((c1 - t0) < kTile ? (c1 - t0) : kTile);
+        __syncthreads();  // the previous tile's compares are done (and suf is written)
+        for (int i = tid; i < kMaxN + n_here; i += kThreads) {
+            const long long src = t0 - kMaxN + i;
+            if (src >= 0) cp_async_4(buf + i, ctx + src);
+            else buf[i] = 0;
         }
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
         __syncthreads();
+        // four candidate ends per 16-byte read, each first tested against the context's last token;
+        // only those that match it (rare) are extended backwards
+        const int32_t last = suf[0];
+        for (int i4 = tid * 4; i4 < n_here; i4 += kThreads * 4) {
+            const int4 w = *reinterpret_cast<const int4 *>(buf + kMaxN + i4);
+            const int32_t v[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int j = 0; j < kPerThread; ++j) buf[kMaxN + j * kThreads + tid] = v[j];
-        __syncthreads();
-#pragma unroll
-        for (int j = 0; j < kPerThread; ++j) {  // independent loads of the next tile, in flight during the compares
-            const long long i = t0 + kTile + j * kThreads + tid;
-            v[j] = i < L ? ctx[i] : 0;
-        }
-        for (int i = tid; i < n_here; i += kThreads) {
-            const long long e = t0 + i;
-            const int lim = static_cast<int>(e + 1 < n_max ? e + 1 : n_max);
-            int m = 0;
-            while (m < lim && buf[kMaxN + i - m] == suf[m]) ++m;
-            if (m >= n_min) {
-                const unsigned long long key = (static_cast<unsigned long long>(m) << 32) | static_cast<unsigned long long>(e);
-                best = key > best ? key : best;
+            for (int q = 0; q < 4; ++q) {
+                const int i = i4 + q;
+                if (i < n_here && v[q] == last) {
+                    const long long e = t0 + i;
+                    const int lim = static_cast<int>(e + 1 < n_max ? e + 1 : n_max);
+                    int m = 1;
+                    while (m < lim && buf[kMaxN + i - m] == suf[m]) ++m;
+                    if (m >= n_min) {
+                        const unsigned long long key =
+                            (static_cast<unsigned long long>(m) << 32) | static_cast<unsigned long long>(e);
+                        best = key > best ? key : best;
+                    }
+                }
             }
         }
     }
@@ -91,10 +106,16 @@ __global__ void __launch_bounds__(kThreads) ngram_kernel(const int32_t *tokens, 
             const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
             best = y > best ? y : best;
         }
-        if (lane == 0) s_best[0] = best;
     }
-    __syncthreads();
-    best = s_best[0];
+    cluster_wait();  // every CTA of the cluster runs: the first one's shared memory is valid
+    if (tid == 0)
+        st_dsmem_f32x2(reinterpret_cast<float2 *>(&s_keys[part]), __uint_as_float(static_cast<uint32_t>(best)),
+                       __uint_as_float(static_cast<uint32_t>(best >> 32)), 0);
+    cluster_sync();  // the keys are in; no CTA touches another's shared memory after this
+    if (part != 0) return;
+    best = 0ull;
+#pragma unroll
+    for (int i = 0; i < kSplit; ++i) best = s_keys[i] > best ? s_keys[i] : best;
     long long k = 0, e_w = -1;
     if (best != 0ull) {
         e_w = static_cast<long long>(best & 0xffffffffull);
@@ -120,14 +141,18 @@ extern "C" sv_status spec_ngram_draft(const int32_t *tokens, const int32_t *ctx_
     }
     if (!tokens || !ctx_offsets || !k_out || (K > 0 && !draft_out)) return SV_ERR_INVALID;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(B);
+    cfg.gridDim = dim3(B, ng::kSplit);
     cfg.blockDim = dim3(ng::kThreads);
     cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;  // the kSplit CTAs of a request form one cluster
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = ng::kSplit;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     const cudaError_t e =
         cudaLaunchKernelEx(&cfg, ng::ngram_kernel, tokens, ctx_offsets, K, n_min, n_max, draft_out, k_out);
     set_launches(1);
