@@ -42,8 +42,8 @@ WORKLOAD = "sampling verify B=64 K=4 V=128256 fp32 logits T=0.7"
 L2_BYTES = 129 << 20
 L2_FLUSH_BYTES = 256 << 20
 NOMINAL_PEAK_GBS = 8000.0
-SUSTAIN_S = 2.0          # headline: seconds of back-to-back steps ahead of the timed K steps
-SUSTAIN_S_OTHER = 0.4    # every other workload
+SUSTAIN_S = 2.0          # headline: seconds of back-to-back steps ahead of the timed K steps (--sustain)
+SUSTAIN_S_OTHER = 0.4    # every other workload (scaled with --sustain)
 
 
 def _peaks():
@@ -197,10 +197,16 @@ def _time_back_to_back(fn, n, stream):
     return e0.elapsed_time(e1) / n
 
 
+_SUSTAIN_SCALE = [1.0]
+
+
 def _sustain(fn, stream, seconds, calls_per_fn=1):
     """About `seconds` of back-to-back calls of fn (the steps of the timed
     region, or a graph replaying them), so that the clock record holds samples
-    under load; returns its own step time."""
+    under load; returns its own step time (None when --sustain 0)."""
+    seconds *= _SUSTAIN_SCALE[0]
+    if seconds <= 0:
+        return None
     t1 = _time_back_to_back(fn, 3, stream)
     n = max(3, min(200000, int(seconds * 1e3 / max(t1, 1e-4))))
     ms = _time_back_to_back(fn, n, stream)
@@ -1188,12 +1194,17 @@ def main():
     ap.add_argument("--l2-flush", action="store_true",
                     help="write a 256 MB buffer before every timed step (its dirty lines are written back "
                          "during the next step); by default the inputs, larger than L2, stand in for a flush")
+    ap.add_argument("--sustain", type=float, default=SUSTAIN_S,
+                    help="seconds of back-to-back headline steps run ahead of the timed steps so that the clock "
+                         "record holds samples under load (the other workloads get a fifth of it); 0 skips them, "
+                         "e.g. under a profiler.  The timed steps are the same either way")
     ap.add_argument("--copies", type=int, default=3,
                     help="resident copies of the inputs the back-to-back steps rotate over (no flush)")
     ap.add_argument("--config", choices=["all", "sampling"] + list(OTHER), default="all",
                     help="all (default): the headline workload's line with every other workload under "
                          "'workloads'; sampling: the headline alone; any other name: that workload alone")
     args = ap.parse_args()
+    _SUSTAIN_SCALE[0] = args.sustain / SUSTAIN_S if SUSTAIN_S > 0 else 0.0
     if args.impl == "reference":
         return run_reference(args)
     if args.config in OTHER:
