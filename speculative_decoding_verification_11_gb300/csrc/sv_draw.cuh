@@ -128,6 +128,8 @@ __device__ __forceinline__ DS ds_shfl(DS a, int src) {
 __device__ __forceinline__ TileScan warp_seg_scan(const float (&r)[2][4], int g, int V, DS base_p, DS t, int lane) {
     float base = 0.f;
     TileScan res{-1, 0.f, 0.f};
+    // base_p + x > t is tested as x > t - base_p, formed once per segment
+    const DS d = ds_add(t, DS{-base_p.hi, -base_p.lo});
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         float pre[4];
@@ -149,7 +151,7 @@ __device__ __forceinline__ TileScan warp_seg_scan(const float (&r)[2][4], int g,
         const int e0 = g * kSegElems + (j * 32 + lane) * 4;
 #pragma unroll
         for (int k = 3; k >= 0; --k)
-            if (e0 + k < V && ds_gt(ds_add_f(base_p, __fadd_rn(head, pre[k])), t)) cand = k;
+            if (e0 + k < V && ds_gt(DS{__fadd_rn(head, pre[k]), 0.f}, d)) cand = k;
         const unsigned m = __ballot_sync(0xffffffffu, cand >= 0);
         if (m && res.v < 0) {
             const int src = __ffs(m) - 1;

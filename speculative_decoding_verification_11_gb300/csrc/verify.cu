@@ -1056,11 +1056,20 @@ __device__ bool fused_draw(const Args &a, int b, const Sel &sel, float invS, int
     }
     DS sum{0.f, 0.f};
     if (in_regs) {
+        // the lane's masses summed pairwise: four levels of independent double-single adds rather
+        // than a chain of sixteen (the draw waits on this sum)
+        static_assert(kRegSeg == 16, "pairwise sum of 16 masses");
+        DS s8[8];
 #pragma unroll
-        for (int i = 0; i < kRegSeg; ++i) {
+        for (int i = 0; i < kRegSeg; ++i)
             if (i0 + i < i1) wmass[i0 + i] = mv[i];
-            sum = ds_add_f(sum, mv[i]);
-        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s8[i] = ds_two_sum(mv[2 * i], mv[2 * i + 1]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s8[i] = ds_add(s8[2 * i], s8[2 * i + 1]);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) s8[i] = ds_add(s8[2 * i], s8[2 * i + 1]);
+        sum = ds_add(s8[0], s8[1]);
         __syncwarp();
     } else {
         for (int i = i0; i < i1; ++i) sum = ds_add_f(sum, dec_mass(ld_relaxed_u32(mw + i)));
