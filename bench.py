@@ -465,10 +465,12 @@ def run_ours(args):
     nominal = W.nominal_bytes(batch)
     logits_bytes = R * V * 4
     gathers = Bn * K * 16 + R * 4 + Bn * 4
-    # one fused kernel runs the whole step: logits once, the drafts' gathers,
-    # and the q row of every request that rejected (re-reading the selected
-    # logits row for the residual is the method's second pass, not counted)
-    step_alg = logits_bytes + gathers + n_reject * V * 4
+    # one fused kernel runs the whole step.  Algorithmic bytes (the scope table's per-step figure):
+    # every logit once, the drafts' gathers, and per request its selected logits row (the residual
+    # or bonus pass needs the row's normaliser first, so the method reads that row twice) and, after
+    # a rejection, that position's q row
+    strict_alg = logits_bytes + gathers + n_reject * V * 4
+    step_alg = strict_alg + Bn * V * 4
     kernel_alg = step_alg
 
     # end to end through the public API: pinned host inputs in, results out
@@ -508,6 +510,8 @@ def run_ours(args):
         "frac_of_8tbs_nominal": nominal / (ms * 1e-3) / 1e9 / NOMINAL_PEAK_GBS,
         "step_algorithmic_bytes": step_alg,
         "step_gbs_algorithmic": step_alg / (ms * 1e-3) / 1e9,
+        "step_bytes_one_pass": strict_alg,
+        "frac_one_pass": strict_alg / (kms * 1e-3) / 1e9 / _peaks()[0],
         "mean_accept_len": float(al_h.float().mean()),
         "emitted_tokens_per_s": world * float(al_h.sum()) / (ms * 1e-3),
         "roofline": _roof("fused_kernel (whole step)", kernel_alg, kms, _traffic("fused_kernel")),
@@ -533,16 +537,20 @@ def run_ours(args):
 # The other verification workloads
 # ---------------------------------------------------------------------------
 def _alg_bytes(batch, al, n_rows_out):
-    """Algorithmic bytes of one verification call: every logit once, 16 B per
-    draft (z[x], q[x], x, u), the q row of every request that rejected (its
-    residual), and 4 B per output row and request."""
+    """Algorithmic bytes of one verification call (the scope table's figure):
+    every logit once, 16 B per draft (z[x], q[x], x, u), 4 B per output row and
+    request, and in sampling mode each request's selected logits row a second
+    time (the residual or bonus pass needs the row's normaliser first) plus the
+    q row of every request that rejected."""
     import torch
     esize = 2 if batch.logits.dtype == torch.bfloat16 else 4
     R, V = batch.rows, batch.V
     nq = R - batch.B
     k_i = (batch.row_offsets[1:] - batch.row_offsets[:-1] - 1).to(al.device)
-    rejected = int((al.to(torch.int64) <= k_i).sum()) if batch.q is not None else 0
-    return R * V * esize + nq * 16 + rejected * V * 4 + (n_rows_out + batch.B) * 4
+    sampling = batch.q is not None
+    rejected = int((al.to(torch.int64) <= k_i).sum()) if sampling else 0
+    second = batch.B * V * esize if sampling else 0
+    return R * V * esize + nq * 16 + second + rejected * V * 4 + (n_rows_out + batch.B) * 4
 
 
 KERNEL_NAMES = {"small": "sk::small_kernel", "cluster": "cv::cluster_kernel", "stream": "fused_kernel",
