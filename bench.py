@@ -72,7 +72,7 @@ KERNEL_SOURCES = {
 }
 KERNEL_SOURCES["fused_kernel_ragged"] = KERNEL_SOURCES["fused_kernel"]  # the same kernel, its ragged capture
 KERNEL_SOURCES["lmhead_gemm_kernel_draft"] = KERNEL_SOURCES["lmhead_gemm_kernel"]  # the draft head's capture
-KERNEL_SOURCES["ngram_kernel"] = ("ngram.cu", "sv_device.cuh", "sv_host.h")
+KERNEL_SOURCES["ngram_kernel"] = ("ngram.cu", "sv_args.cuh", "sv_device.cuh", "sv_host.h")
 
 
 def _source_hash(kernel: str):

@@ -232,7 +232,7 @@ sv_status spec_lmhead_logits(const void *hidden, const void *w_vocab_t, int d, i
  * Speculative Decoding for Faster LLM Inference", Table 1: suffix / n-gram
  * drafting matches strings over the token stream, no model, one lookup).
  * Request b's context is tokens[ctx_offsets[b] .. ctx_offsets[b+1]) (int32,
- * CSR, device).  For n = n_max down to n_min, the context's last n tokens are
+ * CSR, device; `tokens` 4-byte aligned, else SV_ERR_INVALID).  For n = n_max down to n_min, the context's last n tokens are
  * looked up among earlier windows that end before its last token; at the
  * first n with a match, the latest such window wins and the up to K tokens
  * that follow it are proposed (fewer when the context ends first).  Outputs:

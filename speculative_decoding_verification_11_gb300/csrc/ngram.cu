@@ -9,88 +9,239 @@
 // One cluster of kSplit CTAs per request: CTA s of the cluster takes the
 // s-th quarter of the candidate end positions e <= L - 2 and measures, for
 // each, m(e), the length of the common suffix of ctx[..e] and ctx[..L-1] (at
-// most min(n_max, e + 1)); its range of the context (with the kMaxN tokens
-// before it) passes through shared memory in tiles of kTile tokens, copied
-// asynchronously.  The winner maximises (m, e) with m >= n_min: the longest
-// suffix first, then its latest occurrence -- the order in which the method
-// tries n = n_max .. n_min and scans back from the end.  Each CTA's best
-// (m, e) goes to the first CTA of the cluster through distributed shared
-// memory; that CTA writes the proposal.  Splitting a context over four CTAs
-// divides its copy latency and its compares by four; the compares read four
-// candidate ends at a time and test them against the context's last token
-// first, so that only the few that match it are extended.
+// most min(n_max, e + 1)).  The winner maximises (m, e) with m >= n_min: the
+// longest suffix first, then its latest occurrence -- the order in which the
+// method tries n = n_max .. n_min and scans back from the end.  Each CTA's
+// best (m, e) goes to the first CTA of the cluster through distributed shared
+// memory; that CTA writes the proposal.
+//
+// Data movement: a CTA's range passes through a ring of kStages shared-memory
+// stages of kSeg candidate ends each (with the kHalo tokens before them), all
+// stages in flight from the start.  A stage's 16-byte-aligned interior comes
+// with one bulk copy completing on the stage's mbarrier; the at most three
+// tokens on either side of it come with plain loads.  A stage holds token x
+// at index x - (t0 - kHalo) + off, where off puts every token at the same
+// position modulo 16 bytes in shared memory as in global memory, so the bulk
+// copy's two ends are aligned whatever the context's start.  A warp tests 256
+// candidate ends per pass against the context's last token (two 16-byte
+// shared-memory loads per lane, one vote); only a pass holding a match ballots
+// its matches and extends them backwards, one per lane.
 #include <cstdint>
 
 #include "../../include/specverify.h"
+#include "sv_args.cuh"
 #include "sv_device.cuh"
 #include "sv_host.h"
 
 namespace sv {
 namespace ng {
 
-constexpr int kSplit = 4;       // CTAs per request (one cluster)
+constexpr int kSplit = 4;      // CTAs per request (one cluster)
 constexpr int kThreads = 256;
 constexpr int kMaxN = 32;
-constexpr int kTile = 4096;     // candidate ends (and context tokens) staged in shared memory at a time
+constexpr int kHalo = kMaxN;   // tokens staged before a stage's first candidate end (an extension reads 31)
+constexpr int kSeg = 2048;     // candidate ends per stage
+constexpr int kStages = 3;
+// a stage: up to 3 tokens of alignment offset, the halo, kSeg ends, and the last 16-byte group the
+// compares read past the final end
+constexpr int kStageElems = kHalo + kSeg + 8;
+static_assert(kStageElems % 4 == 0, "stages stay 16-byte aligned");
+static_assert(kStages + 2 <= kThreads / 32, "one warp per stage for its ragged ends, one for the suffix");
+constexpr unsigned long long kFailKey = ~0ull;  // a CTA whose copy never landed (no real key has m = 2^32 - 1)
 
-__device__ __forceinline__ void cp_async_4(int32_t *dst, const int32_t *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+struct Stage {
+    int t0;        // first candidate end
+    int n;         // candidate ends in the stage
+    int off;       // shared-memory position of token t0 - kHalo
+};
+
+__device__ __forceinline__ Stage stage_of(int c0, int c1, int g, int phase) {
+    Stage st;
+    st.t0 = c0 + g * kSeg;
+    st.n = (c1 - st.t0) < kSeg ? (c1 - st.t0) : kSeg;
+    st.off = (phase + st.t0 - kHalo) & 3;
+    return st;
 }
 
-__global__ void __launch_bounds__(kThreads) ngram_kernel(const int32_t *tokens, const int32_t *ctx_offsets, int K,
+// Stage st's tokens [max(0, t0 - kHalo), t0 + n) split into a 16-byte-aligned interior [a, b), copied
+// in bulk, and at most six tokens on its two sides, loaded plainly.
+struct Span {
+    int x_lo, a, b, x_hi, shift;  // shared index of token x = x + shift
+};
+
+__device__ __forceinline__ Span span_of(const Stage &st, int phase) {
+    Span p;
+    const int base = st.t0 - kHalo;
+    p.x_lo = base > 0 ? base : 0;
+    p.x_hi = st.t0 + st.n;
+    p.a = p.x_lo + ((4 - ((phase + p.x_lo) & 3)) & 3);  // first aligned token
+    p.b = p.x_hi - ((phase + p.x_hi) & 3);              // end of the aligned interior
+    if (p.a >= p.b) p.a = p.b = p.x_hi;                 // no interior: every token by plain loads
+    p.shift = st.off - base;
+    return p;
+}
+
+// One thread: the interior's bulk copy, completing the stage's mbarrier phase (an arrival alone when
+// there is no interior).
+__device__ __forceinline__ void issue_bulk(int32_t *buf, uint64_t *bar, const int32_t *ctx, const Span &p) {
+    if (p.a < p.b) {
+        const uint64_t policy = l2_evict_first_policy();  // each context token is read once
+        const uint32_t bytes = static_cast<uint32_t>(p.b - p.a) * 4u;
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s_hint(buf + (p.a + p.shift), ctx + p.a, bytes, bar, policy);
+    } else {
+        mbar_arrive(bar);
+    }
+}
+
+// One warp: the tokens on both sides of the interior (lanes 0-7 before it, 8-15 after it).
+__device__ __forceinline__ void load_ends(int32_t *buf, const int32_t *ctx, const Span &p, int lane) {
+    const int head = p.a - p.x_lo, tail = p.x_hi - p.b;
+    if (lane < head) buf[p.x_lo + lane + p.shift] = ctx[p.x_lo + lane];
+    else if (lane >= 8 && lane - 8 < tail) buf[p.b + (lane - 8) + p.shift] = ctx[p.b + (lane - 8)];
+}
+
+// Position of the n-th (from 0) set bit of m; n < popc(m).
+__device__ __forceinline__ int nth_set_bit(unsigned m, int n) {
+    int pos = 0;
+#pragma unroll
+    for (int w = 16; w > 0; w >>= 1) {
+        const unsigned lo = m & ((1u << w) - 1u);
+        const int c = __popc(lo);
+        if (n >= c) {
+            n -= c;
+            m >>= w;
+            pos += w;
+        } else {
+            m = lo;
+        }
+    }
+    return pos;
+}
+
+// The candidate ends of the 32 groups from gw that equal the last token, extended backwards one per lane
+// (slot-major, then lane order), their (m, e) keys folded into best.  Called by a whole warp.
+__device__ __forceinline__ void extend_matches(const int32_t *buf, int gw, int g_end, const Stage &st,
+                                               const int32_t *suf, int n_min, int n_max, int lane,
+                                               unsigned long long &best) {
+    const int gi = gw + lane;
+    const int32_t last = suf[0];
+    const int4 w = gi < g_end ? reinterpret_cast<const int4 *>(buf)[gi] : make_int4(~last, ~last, ~last, ~last);
+    const int i0 = 4 * gi - kHalo - st.off;  // candidate index of slot 0
+    const unsigned m0 = __ballot_sync(0xffffffffu, i0 >= 0 && i0 < st.n && w.x == last);
+    const unsigned m1 = __ballot_sync(0xffffffffu, i0 + 1 >= 0 && i0 + 1 < st.n && w.y == last);
+    const unsigned m2 = __ballot_sync(0xffffffffu, i0 + 2 >= 0 && i0 + 2 < st.n && w.z == last);
+    const unsigned m3 = __ballot_sync(0xffffffffu, i0 + 3 >= 0 && i0 + 3 < st.n && w.w == last);
+    const int p1 = __popc(m0), p2 = p1 + __popc(m1), p3 = p2 + __popc(m2), cnt = p3 + __popc(m3);
+    for (int r = lane; r < cnt; r += 32) {
+        // the r-th match in (slot, lane) order
+        const int q = (r >= p1) + (r >= p2) + (r >= p3);
+        const unsigned mq = q == 0 ? m0 : q == 1 ? m1 : q == 2 ? m2 : m3;
+        const int rq = r - (q == 0 ? 0 : q == 1 ? p1 : q == 2 ? p2 : p3);
+        const int pos = 4 * (gw + nth_set_bit(mq, rq)) + q;
+        const int e = st.t0 + (pos - kHalo - st.off);
+        const int lim = e + 1 < n_max ? e + 1 : n_max;
+        int m = 1;
+        while (m < lim && buf[pos - m] == suf[m]) ++m;
+        if (m >= n_min) {
+            const unsigned long long key = (static_cast<unsigned long long>(m) << 32) | static_cast<unsigned long long>(e);
+            best = key > best ? key : best;
+        }
+    }
+}
+
+// One stage's compares by one warp: 64 groups (256 candidate ends) per pass, two 16-byte loads per lane
+// and one vote; only a pass holding a value equal to the last token (rare) goes on to the per-slot
+// ballots.
+__device__ __forceinline__ unsigned long long compare_stage(const int32_t *buf, Stage st, const int32_t *suf,
+                                                         int n_min, int n_max, int g_end, int warp, int lane,
+                                                         unsigned long long best) {
+    const int32_t last = suf[0];
+    for (int gw = (kHalo >> 2) + warp * 64; gw < g_end; gw += 64 * (kThreads / 32)) {
+        const int ga = gw + lane, gb = ga + 32;
+        const int4 no = make_int4(~last, ~last, ~last, ~last);
+        const int4 wa = ga < g_end ? reinterpret_cast<const int4 *>(buf)[ga] : no;
+        const int4 wb = gb < g_end ? reinterpret_cast<const int4 *>(buf)[gb] : no;
+        const bool hit = (wa.x == last) | (wa.y == last) | (wa.z == last) | (wa.w == last) | (wb.x == last) |
+                         (wb.y == last) | (wb.z == last) | (wb.w == last);
+        if (__any_sync(0xffffffffu, hit)) {
+            extend_matches(buf, gw, g_end, st, suf, n_min, n_max, lane, best);
+            extend_matches(buf, gw + 32, g_end, st, suf, n_min, n_max, lane, best);
+        }
+    }
+    return best;
+}
+
+__global__ void __launch_bounds__(kThreads, 8) ngram_kernel(const int32_t *tokens, const int32_t *ctx_offsets, int K,
                                                          int n_min, int n_max, int32_t *draft_out, int32_t *k_out) {
-    cluster_arrive_relaxed();  // matched by the wait before the first remote store
-    pdl_wait_prior_grid();
-    pdl_launch_dependents();
-    // buf[kMaxN + i] = ctx[t0 + i]; buf[0 .. kMaxN) = the kMaxN tokens before the tile (zero before ctx[0])
-    __shared__ __align__(16) int32_t buf[kMaxN + kTile + 4];
+    __shared__ __align__(16) int32_t ring[kStages][kStageElems];
+    __shared__ __align__(8) uint64_t full[kStages];
     __shared__ int32_t suf[kMaxN];
     __shared__ unsigned long long s_best[kThreads / 32];
     __shared__ unsigned long long s_keys[kSplit];  // the first CTA: every CTA's best key
-    const int b = blockIdx.x, part = static_cast<int>(cluster_ctarank());
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const long long s0 = ctx_offsets[b];
-    long long L = static_cast<long long>(ctx_offsets[b + 1]) - s0;
-    if (L < 0) L = 0;  // decreasing offsets: an empty context, nothing proposed
+    cluster_arrive_relaxed();  // matched by the wait before the first remote store
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_wait_prior_grid();
+    pdl_launch_dependents();
+    const int b = blockIdx.x, part = static_cast<int>(cluster_ctarank());
+    const int s0 = ctx_offsets[b];
+    const int e0 = ctx_offsets[b + 1];
+    const int L = e0 > s0 ? e0 - s0 : 0;  // decreasing offsets: an empty context, nothing proposed
     const int32_t *ctx = tokens + s0;
-    if (tid < n_max && tid < L) suf[tid] = ctx[L - 1 - tid];
-    const long long n_cand = L >= 2 ? L - 1 : 0;  // candidate ends 0 .. L - 2
-    const long long chunk = (n_cand + kSplit - 1) / kSplit;
-    const long long c0 = part * chunk, c1 = (c0 + chunk < n_cand) ? c0 + chunk : n_cand;
+    // 4-byte units of ctx[0]'s address modulo 4 (the pointer is 4-byte aligned: checked on the host)
+    const int phase = static_cast<int>(((reinterpret_cast<uintptr_t>(tokens) >> 2) + static_cast<uintptr_t>(s0)) & 3);
+    const int n_cand = L >= 2 ? L - 1 : 0;  // candidate ends 0 .. L - 2
+    const int chunk = n_cand / kSplit + (n_cand % kSplit != 0);
+    const int c0 = part * chunk < n_cand ? part * chunk : n_cand;
+    const int c1 = c0 + chunk < n_cand ? c0 + chunk : n_cand;
+    const int n_seg = (c1 - c0) / kSeg + ((c1 - c0) % kSeg != 0);
+    // fill the ring: thread 0 issues the bulk copies first; warps 1-3 load the stages' ragged ends and
+    // warp 4 the context's suffix, in parallel
+    if (tid == 0)
+        for (int g = 0; g < n_seg && g < kStages; ++g)
+            issue_bulk(ring[g], &full[g], ctx, span_of(stage_of(c0, c1, g, phase), phase));
+    if (warp >= 1 && warp <= kStages && warp - 1 < n_seg)
+        load_ends(ring[warp - 1], ctx, span_of(stage_of(c0, c1, warp - 1, phase), phase), lane);
+    if (warp == kStages + 1 && lane < n_max && lane < L) suf[lane] = ctx[L - 1 - lane];
     // key = m << 32 | e, 0 = no candidate (m >= n_min >= 1 makes every real key nonzero)
     unsigned long long best = 0ull;
-    for (long long t0 = c0; t0 < c1; t0 += kTile) {
-        const int n_here = static_cast<int>((c1 - t0) < kTile ? (c1 - t0) : kTile);
-        __syncthreads();  // the previous tile's compares are done (and suf is written)
-        for (int i = tid; i < kMaxN + n_here; i += kThreads) {
-            const long long src = t0 - kMaxN + i;
-            if (src >= 0) cp_async_4(buf + i, ctx + src);
-            else buf[i] = 0;
+    int g = 0;
+    bool ok = true;
+    for (; g < n_seg; ++g) {
+        const int s = g % kStages;
+        // the stage's bulk copy (issued by this CTA) and, after the barrier, its plain loads; one thread
+        // polls the mbarrier, the others wait at the barrier without taking issue slots from the SM's
+        // other CTAs
+        const bool landed = tid != 0 || mbar_wait_bounded(&full[s], (g / kStages) & 1, kDrainBudget);
+        if (!__syncthreads_and(landed)) {
+            ok = false;
+            break;
         }
-        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        const Stage st = stage_of(c0, c1, g, phase);
+        const int32_t *buf = ring[s];
+        const int g_end = (kHalo + st.off + st.n + 3) >> 2;  // 16-byte groups holding the stage's ends
+        best = compare_stage(buf, st, suf, n_min, n_max, g_end, warp, lane, best);
+        __syncthreads();  // every compare of stage s is done: it may be refilled
+        if (g + kStages < n_seg) {
+            const Span p = span_of(stage_of(c0, c1, g + kStages, phase), phase);
+            if (tid == 0) issue_bulk(ring[s], &full[s], ctx, p);
+            if (warp == 1) load_ends(ring[s], ctx, p, lane);
+        }
+    }
+    if (!ok) {
+        // a copy did not land within the drain limit: wait once more (bounded) for it and for this
+        // CTA's later copies in flight, then report the request as failed to the first CTA (it
+        // proposes nothing)
+        const int issued = n_seg < g + kStages ? n_seg : g + kStages;
+        if (tid == 0)
+            for (int h = g; h < issued; ++h) mbar_wait_bounded(&full[h % kStages], (h / kStages) & 1, kDrainBudget);
         __syncthreads();
-        // four candidate ends per 16-byte read, each first tested against the context's last token;
-        // only those that match it (rare) are extended backwards
-        const int32_t last = suf[0];
-        for (int i4 = tid * 4; i4 < n_here; i4 += kThreads * 4) {
-            const int4 w = *reinterpret_cast<const int4 *>(buf + kMaxN + i4);
-            const int32_t v[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int i = i4 + q;
-                if (i < n_here && v[q] == last) {
-                    const long long e = t0 + i;
-                    const int lim = static_cast<int>(e + 1 < n_max ? e + 1 : n_max);
-                    int m = 1;
-                    while (m < lim && buf[kMaxN + i - m] == suf[m]) ++m;
-                    if (m >= n_min) {
-                        const unsigned long long key =
-                            (static_cast<unsigned long long>(m) << 32) | static_cast<unsigned long long>(e);
-                        best = key > best ? key : best;
-                    }
-                }
-            }
-        }
+        best = kFailKey;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -116,15 +267,15 @@ __global__ void __launch_bounds__(kThreads) ngram_kernel(const int32_t *tokens, 
     best = 0ull;
 #pragma unroll
     for (int i = 0; i < kSplit; ++i) best = s_keys[i] > best ? s_keys[i] : best;
-    long long k = 0, e_w = -1;
-    if (best != 0ull) {
-        e_w = static_cast<long long>(best & 0xffffffffull);
+    int k = 0, e_w = -1;
+    if (best != 0ull && best != kFailKey) {
+        e_w = static_cast<int>(best & 0xffffffffull);
         k = L - 1 - e_w;
         if (k > K) k = K;
     }
     for (int j = tid; j < K; j += kThreads)
         draft_out[static_cast<size_t>(b) * K + j] = (j < k) ? ctx[e_w + 1 + j] : -1;
-    if (tid == 0) k_out[b] = static_cast<int32_t>(k);
+    if (tid == 0) k_out[b] = k;
 }
 
 }  // namespace ng
@@ -140,6 +291,7 @@ extern "C" sv_status spec_ngram_draft(const int32_t *tokens, const int32_t *ctx_
         return SV_OK;
     }
     if (!tokens || !ctx_offsets || !k_out || (K > 0 && !draft_out)) return SV_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(tokens) & 3u) return SV_ERR_INVALID;  // int32 tokens, 4-byte aligned
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(B, ng::kSplit);
     cfg.blockDim = dim3(ng::kThreads);

@@ -124,6 +124,14 @@ def test_kv_argument_errors_return_before_launch(lib):
     del ok_args
 
 
+def test_ngram_refuses_a_misaligned_token_buffer(lib):
+    """The n-gram drafter's bulk copies need 4-byte-aligned int32 tokens: a
+    pointer off by two bytes is refused before any launch."""
+    P = ctypes.c_void_p(0x1000)
+    assert lib.spec_ngram_draft(ctypes.c_void_p(0x1002), P, 4, 8, 1, 4, P, P, None) == binding.SV_ERR_INVALID
+    assert lib.spec_ngram_draft(P, P, 4, 8, 1, 33, P, P, None) == binding.SV_ERR_INVALID  # n_max
+
+
 def test_noalloc_scratch_size_matches_the_header():
     """The binding's copy of SV_NOALLOC_SCRATCH_BYTES is the header's value."""
     src = open(HEADER).read()

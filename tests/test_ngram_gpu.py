@@ -76,3 +76,29 @@ def test_ngram_argument_errors(cuda_device):
     for n_min, n_max in ((0, 2), (3, 2), (1, 33)):
         with pytest.raises(B_.SpecVerifyError):
             B_.spec_ngram_draft(t, o, 2, n_min, n_max, d, k)
+
+
+@pytest.mark.parametrize("shift", [0, 1, 2, 3])
+def test_long_contexts_at_every_alignment(cuda_device, shift):
+    """Contexts that wrap each CTA's ring of shared-memory stages (several
+    stages per CTA) and start at every 4-byte position of a 16-byte group: the
+    token buffer itself starts `shift` elements into an allocation, and the
+    context lengths are odd, so both ends of each stage's bulk copy fall at
+    every alignment.  Short contexts (no aligned interior at all) sit between
+    them."""
+    dev = cuda_device
+    rng = np.random.default_rng(77 + shift)
+    lens = [2, 3, 4, 5, 6, 7, 8, 9, 31, 33, 8193, 24577, 30001] + rng.integers(10, 40000, size=5).tolist()
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    tokens = rng.integers(0, 3, size=int(offs[-1])).astype(np.int32)
+    full = torch.zeros(len(tokens) + shift, dtype=torch.int32, device=dev)
+    full[shift:] = torch.from_numpy(tokens).to(dev)
+    t = full[shift:]
+    o = torch.from_numpy(offs).to(dev)
+    K, n_min, n_max = 8, 2, 7
+    d = torch.full((len(lens), K), -7, dtype=torch.int32, device=dev)
+    k = torch.full((len(lens),), -7, dtype=torch.int32, device=dev)
+    B_.spec_ngram_draft(t, o, K, n_min, n_max, d, k)
+    torch.cuda.synchronize()
+    od, ok = _oracle(tokens, offs, K, n_min, n_max)
+    assert np.array_equal(k.cpu().numpy(), ok) and np.array_equal(d.cpu().numpy(), od)
