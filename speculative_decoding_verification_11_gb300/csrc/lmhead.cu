@@ -515,8 +515,10 @@ static void launch_gemm_bn(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
 // ---------------------------------------------------------------------------
 constexpr int kDraftThreads = 1024;
 constexpr int kDraftWarps = kDraftThreads / 32;
+static_assert(kDraftWarps == 32, "the warp totals are scanned by one warp");
 constexpr int kMaxDraftSegs = 4096;  // V <= 4096 x 256 tokens
 constexpr uint32_t kDraftStream = 1;  // Philox stream of the draft draws
+constexpr int kDraftBatch = 4;        // segments whose logits a warp loads before using any
 
 // First output word of Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel
 // random numbers: as easy as 1, 2, 3", SC 2011) at counter (index low word,
@@ -556,7 +558,7 @@ __global__ void __launch_bounds__(kDraftThreads) draft_finish_kernel(float *q, c
     const int row = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     __shared__ float2 s_part[kDraftWarps];
     __shared__ float s_segsum[kMaxDraftSegs];
-    __shared__ DS s_wtot[kDraftWarps];
+    __shared__ DS s_wtot[kDraftWarps], s_wincl[kDraftWarps];
     __shared__ int s_owner, s_vstar;
     __shared__ float s_u;
 
@@ -593,29 +595,57 @@ __global__ void __launch_bounds__(kDraftThreads) draft_finish_kernel(float *q, c
     const int G = (ns + kDraftWarps - 1) / kDraftWarps;
     const int g0 = min(warp * G, ns), g1 = min(g0 + G, ns);
 
-    // pass 1: each warp turns its segments into q (in place) and sums them in order
+    // pass 1: each warp turns its segments into q (in place) and sums them in order.  The logits of
+    // kDraftBatch segments are loaded before any is used, so that a warp keeps that many 1 KB reads
+    // in flight (the row comes from L2; one segment at a time left the loads latency-bound).
     DS wt{0.f, 0.f};
-    for (int g = g0; g < g1; ++g) {
-        float r[2][4];
-        seg_load_r<float>(qrow, nullptr, V, g, c, M, invS, lane, r);
+    for (int gb = g0; gb < g1; gb += kDraftBatch) {
+        float4 zb[kDraftBatch][2];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int e0 = g * kSegElems + (j * 32 + lane) * 4;
-            if (e0 < V) *reinterpret_cast<float4 *>(qrow + e0) = make_float4(r[j][0], r[j][1], r[j][2], r[j][3]);
+        for (int b = 0; b < kDraftBatch; ++b)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int e0 = (gb + b) * kSegElems + (j * 32 + lane) * 4;
+                zb[b][j] = (gb + b < g1 && e0 < V) ? __ldcs(reinterpret_cast<const float4 *>(qrow + e0))
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+        for (int b = 0; b < kDraftBatch; ++b) {
+            const int g = gb + b;
+            if (g >= g1) break;
+            float r[2][4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int e0 = g * kSegElems + (j * 32 + lane) * 4;
+                const float z[4] = {zb[b][j].x, zb[b][j].y, zb[b][j].z, zb[b][j].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) r[j][k] = e0 < V ? __fmul_rn(ex2(__fmaf_rn(z[k], c, -M)), invS) : 0.f;
+                if (e0 < V) *reinterpret_cast<float4 *>(qrow + e0) = make_float4(r[j][0], r[j][1], r[j][2], r[j][3]);
+            }
+            const float m = seg_sum(r);
+            if (lane == 0) s_segsum[g] = m;
+            wt = ds_add_f(wt, m);
         }
-        const float m = seg_sum(r);
-        if (lane == 0) s_segsum[g] = m;
-        wt = ds_add_f(wt, m);
     }
     if (lane == 0) s_wtot[warp] = wt;
     __syncthreads();
-    DS R{0.f, 0.f}, Pw{0.f, 0.f};
-    for (int w = 0; w < kDraftWarps; ++w) {
-        if (w < warp) Pw = ds_add(Pw, s_wtot[w]);
-        R = ds_add(R, s_wtot[w]);
+    // inclusive prefix of the warp totals (one warp, shuffle scan), then the owner: the warp whose range
+    // holds u R.  Lower and upper ends of every range come from the same scan, so exactly one warp owns
+    // any u R below the total.
+    if (warp == 0) {
+        DS p = s_wtot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const DS y = ds_shfl_up(p, o);
+            if (lane >= o) p = ds_add(y, p);
+        }
+        s_wincl[lane] = p;
     }
+    __syncthreads();
+    const DS R = s_wincl[kDraftWarps - 1];
+    const DS Pw = warp > 0 ? s_wincl[warp - 1] : DS{0.f, 0.f};
     const DS t = ds_mul_f(R, u);
-    if (lane == 0 && g0 < g1 && !ds_gt(Pw, t) && ds_gt(ds_add(Pw, wt), t)) atomicMin(&s_owner, warp);
+    if (lane == 0 && g0 < g1 && !ds_gt(Pw, t) && ds_gt(s_wincl[warp], t)) atomicMin(&s_owner, warp);
     __syncthreads();
 
     // the owning warp finds the segment, then the token, in token order
@@ -624,7 +654,8 @@ __global__ void __launch_bounds__(kDraftThreads) draft_finish_kernel(float *q, c
         int fseg = -1;
         for (int g = g0; g < g1; ++g) {
             const DS Pn = ds_add_f(P, s_segsum[g]);
-            if (ds_gt(Pn, t)) {
+            // the range holds u R; if its running sum falls short by rounding, its last segment
+            if (ds_gt(Pn, t) || g == g1 - 1) {
                 fseg = g;
                 fbase = P;
                 break;
