@@ -102,3 +102,27 @@ def test_long_contexts_at_every_alignment(cuda_device, shift):
     torch.cuda.synchronize()
     od, ok = _oracle(tokens, offs, K, n_min, n_max)
     assert np.array_equal(k.cpu().numpy(), ok) and np.array_equal(d.cpu().numpy(), od)
+
+
+@pytest.mark.parametrize("n_max", [4, 32])
+def test_dense_matches(cuda_device, n_max):
+    """Contexts where most or all candidate ends equal the last token: a
+    constant context, short periods, and a long periodic run after random
+    tokens (every warp pass holds matches, up to 128 per 32-group block, and
+    the extensions run to n_max).  Lengths span one to several shared-memory
+    stages per CTA."""
+    rng = np.random.default_rng(90 + n_max)
+    ctxs = []
+    for L in (40, 2049, 9000, 30001):
+        ctxs.append(np.full(L, 7, dtype=np.int32))                                   # constant
+        for p in (2, 5, 31):
+            base = rng.integers(0, 1000, size=p).astype(np.int32)
+            ctxs.append(np.resize(base, L))                                          # period p
+        head = rng.integers(0, 1000, size=L // 2).astype(np.int32)
+        ctxs.append(np.concatenate([head, np.resize(np.array([3, 9, 3], np.int32), L - L // 2)]))
+    lens = [len(c) for c in ctxs]
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    tokens = np.concatenate(ctxs).astype(np.int32)
+    d, k = _gpu(cuda_device, tokens, offs, 8, 1, n_max)
+    od, ok = _oracle(tokens, offs, 8, 1, n_max)
+    assert np.array_equal(k, ok) and np.array_equal(d, od)
