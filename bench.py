@@ -330,6 +330,17 @@ def _cpu_sample_all_cores(batch, target_s=10.0):
                       f"{el:.1f} s, fp64 C"}
 
 
+def _headline_config(world, args):
+    """The headline workload's config, the same dict on both arms (the reference arm times the oracle
+    on the workload this arm's GPU steps run, so it reports this arm's config)."""
+    n = 1 if args.l2_flush else args.copies
+    return {"workload": WORKLOAD, "B": 64, "K": 4, "V": 128256, "T": 0.7,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": ("flushed between steps (256 MB write)" if args.l2_flush else
+                   f"no flush: steps run back to back over {n} resident copies of the inputs "
+                   f"({n * 295.5:.0f} MB), so no step reads what the step before it read")}
+
+
 def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
@@ -352,7 +363,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "B": 64, "K": 4, "V": 128256, "T": 0.7},
+            "data": "synthetic", "config": _headline_config(world, args),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": f"{n_req} of 64 requests per step, fp64 C oracle, 1 thread"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -501,11 +512,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": Bn, "K": K, "V": V, "T": T,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": ("flushed between steps (256 MB write)" if args.l2_flush else
-                          f"no flush: steps run back to back over {len(calls)} resident copies of the inputs "
-                          f"({len(calls) * 295.5:.0f} MB), so no step reads what the step before it read")},
+        "config": _headline_config(world, args),
         "hbm_gbs_nominal": world * nominal / (ms * 1e-3) / 1e9,
         "frac_of_8tbs_nominal": nominal / (ms * 1e-3) / 1e9 / NOMINAL_PEAK_GBS,
         "step_algorithmic_bytes": step_alg,
