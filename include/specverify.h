@@ -239,7 +239,9 @@ sv_status spec_lmhead_logits(const void *hidden, const void *w_vocab_t, int d, i
  * draft_out [B x K] int32 (-1 past the proposal), k_out [B] (0..K: the draft
  * length each request proposes, e.g. the K_b of spec_verify_ragged).
  * 1 <= n_min <= n_max <= 32, 0 <= K <= SV_MAX_K.  One kernel on `stream`; a
- * request whose offsets decrease proposes nothing.
+ * request whose offsets decrease, or whose first offset is negative, proposes
+ * nothing and reads no token.  Offsets past the end of `tokens` are not
+ * detected (the buffer's length is not passed): the caller keeps them in range.
  */
 sv_status spec_ngram_draft(const int32_t *tokens, const int32_t *ctx_offsets, int B, int K, int n_min,
                            int n_max, int32_t *draft_out, int32_t *k_out, void *stream);

@@ -191,7 +191,8 @@ __global__ void __launch_bounds__(kThreads, 8) ngram_kernel(const int32_t *token
     const int b = blockIdx.x, part = static_cast<int>(cluster_ctarank());
     const int s0 = ctx_offsets[b];
     const int e0 = ctx_offsets[b + 1];
-    const int L = e0 > s0 ? e0 - s0 : 0;  // decreasing offsets: an empty context, nothing proposed
+    // a negative start or decreasing offsets: an empty context, nothing proposed (and nothing read)
+    const int L = (s0 >= 0 && e0 > s0) ? e0 - s0 : 0;
     const int32_t *ctx = tokens + s0;
     // 4-byte units of ctx[0]'s address modulo 4 (the pointer is 4-byte aligned: checked on the host)
     const int phase = static_cast<int>(((reinterpret_cast<uintptr_t>(tokens) >> 2) + static_cast<uintptr_t>(s0)) & 3);

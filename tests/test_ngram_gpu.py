@@ -67,6 +67,15 @@ def test_decreasing_offsets_propose_nothing(cuda_device):
     assert k[1] == 0 and list(d[1]) == [-1, -1, -1]
 
 
+def test_negative_start_proposes_nothing(cuda_device):
+    """A context whose first offset is negative is empty: nothing proposed,
+    no token read; the next request is unaffected."""
+    tokens = np.array([1, 2, 1, 2, 1, 2], dtype=np.int32)
+    d, k = _gpu(cuda_device, tokens, [-3, 0, 6], 3, 1, 2)
+    assert k[0] == 0 and list(d[0]) == [-1, -1, -1]
+    assert k[1] == 2 and list(d[1]) == [1, 2, -1]
+
+
 def test_ngram_argument_errors(cuda_device):
     dev = cuda_device
     t = torch.zeros(4, dtype=torch.int32, device=dev)
