@@ -73,6 +73,7 @@ KERNEL_SOURCES = {
 KERNEL_SOURCES["fused_kernel_ragged"] = KERNEL_SOURCES["fused_kernel"]  # the same kernel, its ragged capture
 KERNEL_SOURCES["lmhead_gemm_kernel_draft"] = KERNEL_SOURCES["lmhead_gemm_kernel"]  # the draft head's capture
 KERNEL_SOURCES["ngram_kernel"] = ("ngram.cu", "sv_args.cuh", "sv_device.cuh", "sv_host.h")
+KERNEL_SOURCES["small_kernel"] = ("small.cu", "sv_args.cuh", "sv_device.cuh", "sv_draw.cuh", "sv_host.h")
 
 
 def _source_hash(kernel: str):
@@ -655,7 +656,8 @@ def run_config(args, name):
     alg = _alg_bytes(batch, al, R)
     drafts = R - Bn
     traffic = (_traffic("cluster_kernel") if (name == "greedy" and kernel_used == "cluster")
-               else _traffic("fused_kernel_ragged") if (name == "ragged" and kernel_used == "stream") else None)
+               else _traffic("fused_kernel_ragged") if (name == "ragged" and kernel_used == "stream")
+               else _traffic("small_kernel") if (name == "tiny" and kernel_used == "small") else None)
     line = {
         "metric": "verified draft tokens/s", "value": drafts / (ms * 1e-3), "unit": "verified draft tokens/s",
         "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
