@@ -471,18 +471,15 @@ def run_ours(args):
     # outcome of the step (same every step: same inputs)
     al_h = al.cpu()
     out_h_last = out.cpu()
-    n_reject = int((al_h <= K).sum())
     units = Bn * K
     value = _job_value(world, units, ms)
     nominal = W.nominal_bytes(batch)
-    logits_bytes = R * V * 4
-    gathers = Bn * K * 16 + R * 4 + Bn * 4
-    # one fused kernel runs the whole step.  Algorithmic bytes (the scope table's per-step figure):
-    # every logit once, the drafts' gathers, and per request its selected logits row (the residual
-    # or bonus pass needs the row's normaliser first, so the method reads that row twice) and, after
-    # a rejection, that position's q row
-    strict_alg = logits_bytes + gathers + n_reject * V * 4
-    step_alg = strict_alg + Bn * V * 4
+    # one fused kernel runs the whole step.  Algorithmic bytes (the scope table's per-step figure,
+    # _alg_bytes): every logit once, the drafts' gathers, and per request its selected logits row (the
+    # residual or bonus pass needs the row's normaliser first, so the method reads that row twice)
+    # and, after a rejection, that position's q row.  The one-pass count leaves out the second read.
+    step_alg = _alg_bytes(batch, al_h, R)
+    strict_alg = step_alg - Bn * V * 4
     kernel_alg = step_alg
 
     # end to end through the public API: pinned host inputs in, results out
